@@ -1,0 +1,374 @@
+"""Benchmark of the GB300 DFlash2 candidate selector.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--e2e-steps E] [--no-cpu-baseline]
+
+One step is one dflash_selector call over one batch of the workload: vocabulary top-k,
+hidden projection and edge scores, with every input already in HBM. The default
+workload is gemma_large (R=512 requests, S=15 steps, K=32, V=262144, H=5376, rank=256),
+the largest of the five. Its 8.4 GB of inputs per step far exceed the 129 MB L2, so no
+flush is needed between steps.
+
+Rank 0 prints one JSON line. It holds:
+  * value: edge scores per second (R*S*K^2 per step), summed over ranks;
+  * roofline: for the dominant kernel (the top-k scan), its algorithmic bytes per launch
+    over its mean duration, which the library's stage events measure live in the timed
+    region, against the measured HBM peak;
+  * e2e: the same metric through the C ABI with pinned host buffers, host-to-device and
+    device-to-host copies inside the timed region;
+  * cpu_baseline: the CPU oracle, as it stands, on a bounded sample of the workload;
+  * clocks: nvidia-smi samples taken during the timed region.
+With torchrun (N > 1) every rank runs an independent replica on its own GPU and its own
+seed (weak scaling). The only collectives are a barrier and a max over ranks of the time.
+
+--impl reference times the CPU oracle (the reference arm of this benchmark) on a bounded
+sample per step, on the host cores, and prints the same line with "impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from draft_candidate_selector_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "selector edge scores/s (R*S*K^2)"
+UNIT = "edge_scores/s"
+PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_gemma_large.md")
+TOPK_SOURCE = os.path.join(ROOT, "draft_candidate_selector_gb300", "csrc", "topk.cu")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def aggregate(ms_local: float, units_local: int, world: int, group=None) -> tuple[float, float]:
+    """Max over ranks of the step time, and the whole-job throughput (units per second).
+
+    Every rank processes units_local units per step (weak scaling), so the job processes
+    world * units_local units in the slowest rank's time.
+    """
+    t = torch.tensor([ms_local], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend(group) == "nccl":
+            t = t.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    ms_max = float(t.item())
+    return ms_max, world * units_local / (ms_max / 1e3)
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
+    return {"hbm_gbs": 6800.0, "source": "fallback (6.8 TB/s, earlier GB300 measurement)"}
+
+
+def profiled_traffic(workload: str) -> float | None:
+    """DRAM bytes per top-k launch from the committed ncu summary, if it was taken on the
+    current top-k source (its sha256 is recorded with it) and on this workload."""
+    if workload != "gemma_large" or not os.path.exists(PROFILE_TOPK):
+        return None
+    with open(PROFILE_TOPK) as f:
+        text = f.read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_b):
+        return None
+    with open(TOPK_SOURCE, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != m_sha.group(1):
+            return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clocks and throttle reasons."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device: torch.device):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.target = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            self.target = str(device.index or 0)
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="dflash_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i", self.target],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict | None:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != len(self.FIELDS):
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_sample(inp: wl.Inputs, n_req: int, threads: int) -> float:
+    """Seconds the CPU oracle takes for the whole selector on the first n_req requests."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.selector(inp.logits[:n_req], bits(inp.hidden[:n_req]), bits(inp.w_proj),
+                    bits(inp.pred_cb), bits(inp.succ_cb), inp.anchors[:n_req],
+                    inp.workload.K, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp: wl.Inputs, target_s: float = 15.0) -> dict:
+    """The oracle on a bounded sample: requests are added until about target_s of work."""
+    import oracle
+    w = inp.workload
+    threads = oracle.default_threads()
+    t1 = oracle_sample(inp, 1, threads)
+    n = int(max(1, min(w.R, target_s / max(t1, 1e-3))))
+    t = oracle_sample(inp, n, threads) if n > 1 else t1
+    edges = n * w.S * w.K * w.K
+    return {"value": edges / t, "unit": UNIT, "cores": min(threads, n * w.S), "kind": "oracle",
+            "sample": f"{n} of {w.R} requests x {w.S} steps of {w.name} (fp64 CPU oracle, "
+                      f"{t:.1f} s)"}
+
+
+def base_config(w: wl.Workload, world: int) -> dict:
+    return {"workload": w.name, "R": w.R, "S": w.S, "K": w.K, "V": w.V, "H": w.H,
+            "rank": w.rank, "description": w.description,
+            "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, w: wl.Workload) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    threads = oracle.default_threads()
+    inp = wl.make_inputs(w, seed=0)
+    n_req = 1   # one request (S rows) per step keeps --steps K runs within minutes
+    for _ in range(args.warmup):
+        oracle_sample(inp, n_req, threads)
+    times = [oracle_sample(inp, n_req, threads) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    edges = n_req * w.S * w.K * w.K
+    value = edges / (ms / 1e3)
+    sample = f"{n_req} of {w.R} requests x {w.S} steps of {w.name} per step (fp64 CPU oracle)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": base_config(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, n_req * w.S),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, w: wl.Workload) -> None:
+    import draft_candidate_selector_gb300 as ds
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # Inputs: logits are generated straight into pinned host memory (the e2e source).
+    logits_host = torch.empty((w.R, w.S, w.V), dtype=torch.float32, pin_memory=True)
+    inp = wl.make_inputs(w, seed=rank, logits_out=logits_host.numpy())
+    hidden_host = inp.hidden.pin_memory()
+    anchors_host = torch.from_numpy(inp.anchors).pin_memory()
+    logits = logits_host.to(dev)
+    hidden = hidden_host.to(dev)
+    anchors = anchors_host.to(dev)
+    w_proj, pred_cb, succ_cb = inp.w_proj.to(dev), inp.pred_cb.to(dev), inp.succ_cb.to(dev)
+    cand = torch.empty((w.R, w.S, w.K), dtype=torch.int32, device=dev)
+    unary = torch.empty((w.R, w.S, w.K), dtype=torch.float32, device=dev)
+    h = torch.empty((w.R, w.S, w.rank), dtype=torch.bfloat16, device=dev)
+    edges = torch.empty((w.R, w.S, w.K, w.K), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.dflash_selector_workspace_bytes(w.R, w.S, w.V, w.K), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        ds.dflash_selector(logits, hidden, w_proj, pred_cb, succ_cb, anchors, w.K, cand, unary,
+                           h, edges, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ds.dflash_device_status(clear=True)
+
+    # ---- timed region (device-resident inputs)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clocks:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        ds.dflash_trace_begin(args.steps)
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+    stages = ds.dflash_trace_end(args.steps)
+    ms_local = start.elapsed_time(stop) / args.steps
+    status = ds.dflash_device_status(clear=True)
+    ms_max, value = aggregate(ms_local, w.edges_per_call, world)
+
+    # ---- end to end through the public call, with host buffers
+    out_edges = torch.empty(edges.shape, dtype=edges.dtype, pin_memory=True)
+    out_cand = torch.empty(cand.shape, dtype=cand.dtype, pin_memory=True)
+    out_unary = torch.empty(unary.shape, dtype=unary.dtype, pin_memory=True)
+    h2d = logits_host.nbytes + hidden_host.nbytes + anchors_host.nbytes
+    d2h = out_edges.nbytes + out_cand.nbytes + out_unary.nbytes
+
+    def e2e_step():
+        logits.copy_(logits_host, non_blocking=True)
+        hidden.copy_(hidden_host, non_blocking=True)
+        anchors.copy_(anchors_host, non_blocking=True)
+        step()
+        out_edges.copy_(edges, non_blocking=True)
+        out_cand.copy_(cand, non_blocking=True)
+        out_unary.copy_(unary, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1) / args.e2e_steps, w.edges_per_call, world)
+
+    if rank == 0:
+        topk_ms = statistics.mean(s[1] for s in stages)
+        proj_ms = statistics.mean(s[0] for s in stages)
+        edge_ms = statistics.mean(s[2] for s in stages)
+        b = w.algorithmic_bytes()
+        topk_bytes = b["logits"] + b["ids_unary_out"]
+        peaks = measured_peaks()
+        achieved = topk_bytes / (topk_ms / 1e3) / 1e9
+        traffic = profiled_traffic(w.name)
+        total_bytes = sum(b.values())
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 logits / bf16 x bf16 -> f32 projection and edges",
+            "data": "synthetic (seeded, shapes and distributions of the workload)",
+            "config": base_config(w, world),
+            "roofline": {"bound": "hbm", "kernel": "topk_kernel", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes_per_launch": topk_bytes,
+                         "peak_source": peaks["source"]},
+            "fused_hbm": {"algorithmic_bytes_per_step": total_bytes,
+                          "achieved_gbs": total_bytes / (ms_max / 1e3) / 1e9,
+                          "frac": total_bytes / (ms_max / 1e3) / 1e9 / peaks["hbm_gbs"]},
+            "stages_ms": {"projection": proj_ms, "topk": topk_ms, "edges": edge_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "device_status": status,
+            "clocks": clocks.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(inp)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemma_large", choices=wl.WORKLOAD_ORDER)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

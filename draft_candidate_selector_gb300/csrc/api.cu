@@ -1,0 +1,354 @@
+// api.cu: the extern "C" boundary of the selector library (declared in include/dflash.h).
+//
+// This file validates arguments on the host, finds the device facts the launchers need,
+// owns the device status word, and runs the fused selector and its stage tracing. All
+// arithmetic of the method lives in topk.cu, projection.cu and edges.cu.
+#include "dflash.h"
+#include "common.cuh"
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+#include <vector>
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dflash_status fail(dflash_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+dflash_status ok() {
+    g_last_error.clear();
+    return DFLASH_OK;
+}
+
+dflash_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(DFLASH_CUDA_ERROR, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bits the kernels set on problems they detect; read through dflash_device_status.
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceSlot {
+    dflash::DeviceInfo info;
+    uint32_t* status_word = nullptr;
+    bool ready = false;
+};
+
+std::mutex g_dev_mu;
+DeviceSlot g_dev[kMaxDevices];
+
+// Facts about the current device, looked up once per device.
+dflash_status current_device(dflash::DeviceInfo* info, uint32_t** status_word) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(DFLASH_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    if (dev < 0 || dev >= kMaxDevices) return fail(DFLASH_NO_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceSlot& s = g_dev[dev];
+    if (!s.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        if (prop.major != 10 || prop.minor != 3)
+            return fail(DFLASH_NO_DEVICE,
+                        "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
+                        prop.major, prop.minor);
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        s.info.device = dev;
+        s.info.sm_count = prop.multiProcessorCount;
+        s.info.cc_major = prop.major;
+        s.info.cc_minor = prop.minor;
+        s.info.smem_optin = prop.sharedMemPerBlockOptin;
+        s.status_word = static_cast<uint32_t*>(p);
+        s.ready = true;
+    }
+    if (info) *info = s.info;
+    if (status_word) *status_word = s.status_word;
+    return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- argument checks
+
+dflash_status check_dims_topk(int R, int S, int V, int K) {
+    if (R < 1 || S < 1 || V < 1 || K < 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R, S, V and K must be >= 1 (got R=%d S=%d V=%d K=%d)",
+                    R, S, V, K);
+    if (K > V) return fail(DFLASH_INVALID_ARGUMENT, "K=%d exceeds V=%d", K, V);
+    if (K > 32) return fail(DFLASH_UNSUPPORTED, "K=%d: top-k supports K <= 32", K);
+    if ((long long)R * S > (1LL << 31) - 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R*S=%lld rows exceeds 2^31-1", (long long)R * S);
+    return DFLASH_OK;
+}
+
+dflash_status check_rank(int rank) {
+    if (rank < 1) return fail(DFLASH_INVALID_ARGUMENT, "rank=%d must be >= 1", rank);
+    if (rank % 8 != 0 || rank > 256)
+        return fail(DFLASH_UNSUPPORTED, "rank=%d: supported ranks are multiples of 8 up to 256", rank);
+    return DFLASH_OK;
+}
+
+dflash_status check_dims_projection(int R, int S, int H, int rank) {
+    if (R < 1 || S < 1 || H < 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R, S and H must be >= 1 (got R=%d S=%d H=%d)", R, S, H);
+    if (H % 8 != 0) return fail(DFLASH_UNSUPPORTED, "H=%d: must be a multiple of 8", H);
+    if ((long long)R * S > (1LL << 31) - 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R*S=%lld rows exceeds 2^31-1", (long long)R * S);
+    return check_rank(rank);
+}
+
+dflash_status check_dims_edges(int R, int S, int K, int V, int rank) {
+    if (R < 1 || S < 1 || V < 1 || K < 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R, S, V and K must be >= 1 (got R=%d S=%d V=%d K=%d)",
+                    R, S, V, K);
+    if (K > V) return fail(DFLASH_INVALID_ARGUMENT, "K=%d exceeds V=%d", K, V);
+    if (K > 32) return fail(DFLASH_UNSUPPORTED, "K=%d: edges support K <= 32", K);
+    if ((long long)R * S > (1LL << 31) - 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R*S=%lld rows exceeds 2^31-1", (long long)R * S);
+    return check_rank(rank);
+}
+
+dflash_status check_ptr(const void* p, const char* name) {
+    if (!p) return fail(DFLASH_INVALID_ARGUMENT, "%s is NULL", name);
+    if (!aligned16(p)) return fail(DFLASH_INVALID_ARGUMENT, "%s is not 16-byte aligned", name);
+    return DFLASH_OK;
+}
+
+#define DFLASH_TRY(expr)                     \
+    do {                                     \
+        dflash_status _s = (expr);           \
+        if (_s != DFLASH_OK) return _s;      \
+    } while (0)
+
+// ---------------------------------------------------------------- stage tracing
+
+struct Trace {
+    std::mutex mu;
+    int device = -1;
+    int capacity = 0;   // calls
+    int used = 0;
+    std::vector<cudaEvent_t> events;   // 4 per call
+};
+Trace g_trace;
+
+// Event slots for the next traced call, or nullptr when tracing is off or full.
+cudaEvent_t* trace_slot(int device) {
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    if (g_trace.capacity == 0 || g_trace.used >= g_trace.capacity || g_trace.device != device)
+        return nullptr;
+    return &g_trace.events[4 * (g_trace.used++)];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_version(void) { return "0.1.0"; }
+
+const char* dflash_status_string(int status) {
+    switch (status) {
+        case DFLASH_OK: return "DFLASH_OK";
+        case DFLASH_INVALID_ARGUMENT: return "DFLASH_INVALID_ARGUMENT";
+        case DFLASH_UNSUPPORTED: return "DFLASH_UNSUPPORTED";
+        case DFLASH_WORKSPACE_TOO_SMALL: return "DFLASH_WORKSPACE_TOO_SMALL";
+        case DFLASH_CUDA_ERROR: return "DFLASH_CUDA_ERROR";
+        case DFLASH_NO_DEVICE: return "DFLASH_NO_DEVICE";
+        default: return "DFLASH_UNKNOWN_STATUS";
+    }
+}
+
+const char* dflash_last_error(void) { return g_last_error.c_str(); }
+
+size_t dflash_topk_workspace_bytes(int R, int S, int V, int K) {
+    if (check_dims_topk(R, S, V, K) != DFLASH_OK) return 0;
+    dflash::DeviceInfo dev;
+    if (current_device(&dev, nullptr) != DFLASH_OK) return 0;
+    return dflash::topk_plan(dev, (long long)R * S, V).workspace_bytes();
+}
+
+size_t dflash_selector_workspace_bytes(int R, int S, int V, int K) {
+    return dflash_topk_workspace_bytes(R, S, V, K);
+}
+
+dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, int K,
+                                     int32_t* cand_ids, float* unary, void* workspace,
+                                     size_t workspace_bytes, dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_ptr(logits, "logits"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr(workspace, "workspace"));
+    dflash::DeviceInfo dev;
+    DFLASH_TRY(current_device(&dev, nullptr));
+    const dflash::TopkPlan plan = dflash::topk_plan(dev, (long long)R * S, V);
+    if (workspace_bytes < plan.workspace_bytes())
+        return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
+                    workspace_bytes, plan.workspace_bytes());
+    cudaError_t e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return ok();
+}
+
+dflash_status dflash_hidden_projection(const uint16_t* hidden, const uint16_t* w_proj, int R,
+                                       int S, int H, int rank, uint16_t* h_out,
+                                       dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_projection(R, S, H, rank));
+    DFLASH_TRY(check_ptr(hidden, "hidden"));
+    DFLASH_TRY(check_ptr(w_proj, "w_proj"));
+    DFLASH_TRY(check_ptr(h_out, "h_out"));
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    cudaError_t e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    return ok();
+}
+
+dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* succ_cb,
+                                     const int32_t* cand_ids, const float* unary,
+                                     const uint16_t* h, const int32_t* anchors, int R, int S,
+                                     int K, int V, int rank, float* edges,
+                                     dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_edges(R, S, K, V, rank));
+    DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
+    DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr(h, "h"));
+    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_ptr(edges, "edges"));
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    cudaError_t e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h, anchors, R, S,
+                                         K, V, rank, edges, status,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "edges launch");
+    return ok();
+}
+
+dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const uint16_t* w_proj,
+                              const uint16_t* pred_cb, const uint16_t* succ_cb,
+                              const int32_t* anchors, int R, int S, int K, int V, int H, int rank,
+                              int32_t* cand_ids, float* unary, uint16_t* h_out, float* edges,
+                              void* workspace, size_t workspace_bytes, dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_dims_projection(R, S, H, rank));
+    DFLASH_TRY(check_ptr(logits, "logits"));
+    DFLASH_TRY(check_ptr(hidden, "hidden"));
+    DFLASH_TRY(check_ptr(w_proj, "w_proj"));
+    DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
+    DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
+    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr(h_out, "h_out"));
+    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr(workspace, "workspace"));
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    const dflash::TopkPlan plan = dflash::topk_plan(dev, (long long)R * S, V);
+    if (workspace_bytes < plan.workspace_bytes())
+        return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
+                    workspace_bytes, plan.workspace_bytes());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaEvent_t* ev = trace_slot(dev.device);
+    cudaError_t e;
+    if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
+                             rank, edges, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "edges launch");
+    if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    return ok();
+}
+
+dflash_status dflash_device_status(uint32_t* flags, int clear) {
+    if (!flags) return fail(DFLASH_INVALID_ARGUMENT, "flags is NULL");
+    DFLASH_TRY(current_device(nullptr, nullptr));
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMemcpyFromSymbol(flags, g_device_status, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    if (clear) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    }
+    return ok();
+}
+
+dflash_status dflash_trace_begin(int n_calls) {
+    if (n_calls < 1 || n_calls > (1 << 20))
+        return fail(DFLASH_INVALID_ARGUMENT, "n_calls=%d must be in [1, 2^20]", n_calls);
+    dflash::DeviceInfo dev;
+    DFLASH_TRY(current_device(&dev, nullptr));
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    if (g_trace.capacity != 0) return fail(DFLASH_INVALID_ARGUMENT, "a trace is already active");
+    g_trace.events.assign(4 * (size_t)n_calls, nullptr);
+    for (auto& ev : g_trace.events) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) {
+            for (auto& x : g_trace.events)
+                if (x) cudaEventDestroy(x);
+            g_trace.events.clear();
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    g_trace.device = dev.device;
+    g_trace.capacity = n_calls;
+    g_trace.used = 0;
+    return ok();
+}
+
+dflash_status dflash_trace_end(float* stage_ms, int max_calls, int* n_calls) {
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    if (g_trace.capacity == 0) return fail(DFLASH_INVALID_ARGUMENT, "no trace is active");
+    dflash_status st = DFLASH_OK;
+    const int n = g_trace.used < max_calls ? g_trace.used : (max_calls > 0 ? max_calls : 0);
+    for (int i = 0; i < n && st == DFLASH_OK; ++i) {
+        cudaEvent_t* ev = &g_trace.events[4 * (size_t)i];
+        cudaError_t e = cudaEventSynchronize(ev[3]);
+        for (int k = 0; k < 3 && e == cudaSuccess; ++k) {
+            float ms = 0.f;
+            e = cudaEventElapsedTime(&ms, ev[k], ev[k + 1]);
+            if (stage_ms) stage_ms[3 * i + k] = ms;
+        }
+        if (e != cudaSuccess) st = cuda_fail(e, "reading trace events");
+    }
+    for (auto& ev : g_trace.events) cudaEventDestroy(ev);
+    g_trace.events.clear();
+    g_trace.capacity = 0;
+    g_trace.used = 0;
+    g_trace.device = -1;
+    if (n_calls) *n_calls = n;
+    return st == DFLASH_OK ? ok() : st;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// common.cuh: declarations shared by the selector's CUDA translation units.
+//
+// Each kernel file exposes one host launcher. dflash_api.cu validates the arguments and
+// then calls the launchers. Kernels report problems through a device status word whose
+// address api.cu passes in. Nothing here allocates memory.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dflash {
+
+constexpr uint32_t kStatusBadId = 0x1u;     // matches DFLASH_DEVICE_BAD_ID
+constexpr uint32_t kStatusTimeout = 0x2u;   // matches DFLASH_DEVICE_TIMEOUT
+
+// Per-device facts the launchers size their grids with.
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    size_t smem_optin = 0;   // max dynamic shared memory per block (opt-in)
+};
+
+// ---------------------------------------------------------------- top-k (topk.cu)
+
+// How the flat stream of R*S*V logits is cut among warps. Every warp takes one
+// contiguous span of `span` logits (the last one may be shorter). A row split across
+// several warps is merged by whichever of them finishes last.
+struct TopkPlan {
+    long long total = 0;      // R * S * V
+    long long span = 0;       // logits per warp, a multiple of 128
+    int warps = 0;            // warps with work
+    int blocks = 0;           // CTAs launched
+    long long rows = 0;       // R * S
+    size_t counter_bytes = 0; // per-row arrival counters (uint32), padded to 256 B
+    size_t partial_bytes = 0; // two 32-entry partial lists (uint64) per warp
+    size_t workspace_bytes() const { return counter_bytes + partial_bytes; }
+};
+
+TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V);
+
+cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
+                        int32_t* cand_ids, float* unary, void* workspace,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------- projection (projection.cu)
+
+// Returns cudaSuccess, or an error if the tensor maps cannot be encoded or the launch
+// fails. status_word receives kStatusTimeout if a bounded pipeline wait gives up.
+cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
+                              const uint16_t* w_proj, int M, int H, int rank,
+                              uint16_t* h_out, uint32_t* status_word, cudaStream_t stream);
+
+// ---------------------------------------------------------------- edges (edges.cu)
+
+cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
+                         const uint16_t* succ_cb, const int32_t* cand_ids, const float* unary,
+                         const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
+                         int rank, float* edges, uint32_t* status_word, cudaStream_t stream);
+
+}  // namespace dflash

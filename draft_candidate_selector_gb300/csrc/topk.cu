@@ -1,0 +1,303 @@
+// topk.cu: the top-K candidates of every logit row, in one streaming pass.
+//
+// Method: page "vllm.models.beam.nvidia.dflash2", DFlash2BeamForCausalLM.compute_candidates
+// (the selector's top-k candidate ids and their logits at each position). Candidate
+// order: logit descending, then token id ascending; -0 == +0; NaN with the sign clear
+// above +inf, NaN with the sign set below -inf.
+//
+// Design (HBM-bound: every logit is read exactly once, 4 bytes, no re-reads):
+//   * The R*S*V logits form one flat stream. It is cut into equal spans, one per warp
+//     of a single full wave (SMs x resident CTAs x 8 warps). Every warp moves the same
+//     number of bytes, whatever V is, and no CTA waits for a second wave.
+//   * A warp reads its span with 128-bit non-allocating loads, eight in flight per lane
+//     (each warp instruction covers 512 contiguous bytes).
+//   * The warp's running top-K is a sorted list, one entry per lane. An entry is a
+//     64-bit key: an order-preserving transform of the logit bits in the high word, the
+//     complemented token id in the low word. Comparing two keys as integers gives the
+//     candidate order, ties included.
+//   * A float compare against the K-th entry's logit filters almost every element.
+//     It is conservative: NaNs and ties with the threshold value pass. Survivors are
+//     inserted one at a time, with a ballot for the position and a shuffle to shift.
+//   * A row split across warps: each warp writes its sorted list to the workspace and
+//     bumps the row's arrival counter. The warp that arrives last merges the lists with
+//     warp-wide bitonic merges and writes the row. Nobody waits, so nothing can hang.
+#include "common.cuh"
+
+#include <algorithm>
+#include <mutex>
+
+namespace dflash {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerBlock = kThreads / 32;
+constexpr int kUnroll = 8;              // 128-bit loads in flight per lane
+constexpr long long kMinSpan = 4096;    // smallest span given to one warp
+constexpr long long kSpanAlign = 128;   // spans start on 512-byte boundaries
+constexpr unsigned kFull = 0xffffffffu;
+
+// Order-preserving map from float bits to uint32: a larger float gives a larger key.
+// -0 is folded onto +0, and the NaNs of each sign are folded onto one key just outside
+// the infinities.
+__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
+    bits = (bits == 0x80000000u) ? 0u : bits;
+    uint32_t k = bits ^ ((uint32_t)((int32_t)bits >> 31) | 0x80000000u);
+    return min(max(k, 0x007FFFFEu), 0xFF800001u);
+}
+
+// Inverse of order_key (up to the folding of -0 and NaN payloads).
+__device__ __forceinline__ float key_value(uint32_t key) {
+    uint32_t bits = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
+    return __uint_as_float(bits);
+}
+
+__device__ __forceinline__ uint64_t make_entry(float v, uint32_t id) {
+    return ((uint64_t)order_key(__float_as_uint(v)) << 32) | (uint32_t)(~id);
+}
+
+__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
+    uint32_t lo = __shfl_sync(kFull, (uint32_t)v, src);
+    uint32_t hi = __shfl_sync(kFull, (uint32_t)(v >> 32), src);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t shfl_up64(uint64_t v, int d) {
+    uint32_t lo = __shfl_up_sync(kFull, (uint32_t)v, d);
+    uint32_t hi = __shfl_up_sync(kFull, (uint32_t)(v >> 32), d);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
+    uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, m);
+    uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// Streaming 128-bit load: read-only path, no L1 allocation, 256-byte L2 prefetch.
+__device__ __forceinline__ float4 ld_stream(const float4* p) {
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// A warp's running top list: lane i holds the entry of rank i (lane 0 is the best).
+// Lanes at or past K hold leftovers that are never reported.
+struct WarpList {
+    uint64_t e;       // this lane's entry
+    uint64_t thr;     // entry of rank K-1: a newcomer must beat it
+    float thr_f;      // logit of that entry, for the float pre-filter
+};
+
+__device__ __forceinline__ void list_reset(WarpList& L) {
+    L.e = 0;                               // sentinel: below every real entry
+    L.thr = 0;
+    L.thr_f = __uint_as_float(0xFFFFFFFFu);   // NaN: the pre-filter passes everything
+}
+
+// Insert c (uniform across the warp, known to beat L.thr) at its rank.
+__device__ __forceinline__ void list_insert(WarpList& L, uint64_t c, int lane, int K) {
+    const int pos = __popc(__ballot_sync(kFull, L.e > c));
+    const uint64_t up = shfl_up64(L.e, 1);
+    if (lane == pos) L.e = c;
+    else if (lane > pos) L.e = up;
+    L.thr = shfl64(L.e, K - 1);
+    L.thr_f = key_value((uint32_t)(L.thr >> 32));
+}
+
+// Offer every lane's candidate entry to the list, lowest lane first.
+__device__ __forceinline__ void list_offer(WarpList& L, uint64_t c, bool valid, int lane, int K) {
+    unsigned m = __ballot_sync(kFull, valid && c > L.thr);
+    while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const uint64_t x = shfl64(c, src);
+        if (x > L.thr) list_insert(L, x, lane, K);
+    }
+}
+
+// Conservative float pre-filter: false only if all four values surely lose to t.
+__device__ __forceinline__ bool may_enter(const float4& v, float t) {
+    return !(v.x < t) | !(v.y < t) | !(v.z < t) | !(v.w < t);
+}
+
+__device__ __forceinline__ void offer4(WarpList& L, const float4& v, uint32_t col, bool valid,
+                                       int lane, int K) {
+    list_offer(L, make_entry(v.x, col + 0), valid, lane, K);
+    list_offer(L, make_entry(v.y, col + 1), valid, lane, K);
+    list_offer(L, make_entry(v.z, col + 2), valid, lane, K);
+    list_offer(L, make_entry(v.w, col + 3), valid, lane, K);
+}
+
+// The 32 best of two sorted 32-lists: a bitonic merge across the warp.
+__device__ __forceinline__ uint64_t merge_lists(uint64_t a, uint64_t b, int lane) {
+    const uint64_t br = shfl64(b, 31 - lane);
+    uint64_t m = a > br ? a : br;             // bitonic, and holds the 32 best
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const uint64_t o = shfl_xor64(m, s);
+        const bool lower = (lane & s) == 0;
+        m = lower ? (m > o ? m : o) : (m < o ? m : o);
+    }
+    return m;
+}
+
+__device__ __forceinline__ void write_row(uint64_t e, long long row, int lane, int K,
+                                          int32_t* __restrict__ cand_ids,
+                                          float* __restrict__ unary) {
+    if (lane < K) {
+        cand_ids[row * K + lane] = (int32_t)(~(uint32_t)e);
+        unary[row * K + lane] = key_value((uint32_t)(e >> 32));
+    }
+}
+
+// Scan flat logits [lo, hi), all inside the row that starts at flat index row_base.
+__device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict__ logits,
+                                           long long lo, long long hi, long long row_base,
+                                           int lane, int K) {
+    // Unaligned head (fewer than 4 logits; only when V is not a multiple of 4).
+    const long long a4 = min(hi, (lo + 3) & ~3LL);
+    if (lo < a4) {
+        const long long i = lo + lane;
+        const bool valid = i < a4;
+        const float v = valid ? logits[i] : 0.f;
+        list_offer(L, make_entry(v, (uint32_t)(i - row_base)), valid, lane, K);
+    }
+    const long long b4 = max(a4, hi & ~3LL);
+    const float4* __restrict__ p = reinterpret_cast<const float4*>(logits + a4);
+    const long long n4 = (b4 - a4) >> 2;
+    const uint32_t col0 = (uint32_t)(a4 - row_base);
+
+    long long j = 0;
+    for (; j + 32 * kUnroll <= n4; j += 32 * kUnroll) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream(p + j + u * 32 + lane);
+        bool hit = false;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) hit |= may_enter(v[u], L.thr_f);
+        if (__any_sync(kFull, hit)) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (__any_sync(kFull, may_enter(v[u], L.thr_f))) {
+                    const uint32_t col = col0 + (uint32_t)((j + u * 32 + lane) * 4);
+                    offer4(L, v[u], col, true, lane, K);
+                }
+            }
+        }
+    }
+    for (; j < n4; j += 32) {
+        const long long idx = j + lane;
+        const bool valid = idx < n4;
+        const float4 v = valid ? ld_stream(p + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (__any_sync(kFull, valid && may_enter(v, L.thr_f)))
+            offer4(L, v, col0 + (uint32_t)(idx * 4), valid, lane, K);
+    }
+    // Unaligned tail (fewer than 4 logits).
+    if (b4 < hi) {
+        const long long i = b4 + lane;
+        const bool valid = i < hi;
+        const float v = valid ? logits[i] : 0.f;
+        list_offer(L, make_entry(v, (uint32_t)(i - row_base)), valid, lane, K);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+topk_kernel(const float* __restrict__ logits, long long total, long long span, int warps, int V,
+            int K, int32_t* __restrict__ cand_ids, float* __restrict__ unary,
+            uint32_t* __restrict__ counters, uint64_t* __restrict__ partials) {
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (gw >= warps) return;
+    const long long s = gw * span;
+    const long long e = min(total, s + span);
+    const long long r_first = s / V;
+    const long long r_last = (e - 1) / V;
+
+    for (long long r = r_first; r <= r_last; ++r) {
+        const long long row_base = r * V;
+        const long long lo = max(s, row_base);
+        const long long hi = min(e, row_base + V);
+        WarpList L;
+        list_reset(L);
+        scan_range(L, logits, lo, hi, row_base, lane, K);
+
+        // Warps whose spans touch this row.
+        const long long w0 = row_base / span;
+        const long long w1 = (row_base + V - 1) / span;
+        if (w0 == w1) {
+            write_row(L.e, r, lane, K, cand_ids, unary);
+            continue;
+        }
+        // Only a warp's first and last rows can be shared: one slot for each.
+        const int slot = (r == r_first) ? 0 : 1;
+        partials[(gw * 2 + slot) * 32 + lane] = L.e;
+        __threadfence();
+        __syncwarp();
+        unsigned arrived = 0;
+        if (lane == 0) arrived = atomicAdd(&counters[r], 1u);
+        arrived = __shfl_sync(kFull, arrived, 0);
+        if (arrived != (unsigned)(w1 - w0)) continue;   // not the last one: done
+        __threadfence();
+        uint64_t m = L.e;
+        for (long long w = w0; w <= w1; ++w) {
+            if (w == gw) continue;
+            const int ws = (r == (w * span) / V) ? 0 : 1;
+            const uint64_t other = __ldcg(
+                reinterpret_cast<const unsigned long long*>(partials) + (w * 2 + ws) * 32 + lane);
+            m = merge_lists(m, other, lane);
+        }
+        write_row(m, r, lane, K, cand_ids, unary);
+    }
+}
+
+int resident_blocks_per_sm(int device) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return 1;
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_kernel, kThreads, 0) !=
+                cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = 1;
+        }
+        cache[device] = n;
+    }
+    return cache[device];
+}
+
+}  // namespace
+
+TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V) {
+    TopkPlan p;
+    p.rows = rows;
+    p.total = rows * (long long)V;
+    const long long max_warps =
+        (long long)std::max(1, dev.sm_count) * resident_blocks_per_sm(dev.device) * kWarpsPerBlock;
+    long long span = (p.total + max_warps - 1) / max_warps;
+    span = std::max(span, kMinSpan);
+    span = (span + kSpanAlign - 1) / kSpanAlign * kSpanAlign;
+    p.span = span;
+    p.warps = (int)((p.total + span - 1) / span);
+    p.blocks = (p.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    p.counter_bytes = (size_t)((rows * 4 + 255) / 256 * 256);
+    p.partial_bytes = (size_t)p.warps * 2 * 32 * sizeof(uint64_t);
+    return p;
+}
+
+cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
+                        int32_t* cand_ids, float* unary, void* workspace, cudaStream_t stream) {
+    uint32_t* counters = static_cast<uint32_t*>(workspace);
+    uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
+                                                     plan.counter_bytes);
+    cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
+    if (err != cudaSuccess) return err;
+    topk_kernel<<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span, plan.warps,
+                                                      V, K, cand_ids, unary, counters, partials);
+    return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -1,0 +1,167 @@
+/*
+ * dflash.h: C ABI of the GB300 (sm_103a) DFlash2 low-rank candidate selector.
+ *
+ * The method comes from the page "vllm.models.beam.nvidia.dflash2" (DFlash2 draft model
+ * for Beam targets). For request r and block position (step) p, the selector:
+ *   1. takes the top-K vocabulary candidates of the drafter's logits and their logits
+ *      ("unary" scores)                  DFlash2BeamForCausalLM.compute_candidates
+ *   2. projects the drafter hidden state to the codebook rank,
+ *      h_p = W_proj . hidden[r, p]       DFlash2BeamCandidateSelector.__init__ / forward
+ *   3. scores every candidate c against every candidate q one position back,
+ *      E[r,p,q,c] = unary[r,p,c] + <pred_cb[cand[r,p-1,q]] * h_p, succ_cb[cand[r,p,c]]>,
+ *      where the predecessor at p = 0 is the request's anchor token.
+ *                                        DFlash2BeamCandidateSelector (class docstring)
+ *
+ * Conventions for every entry point:
+ *   - Pointers are caller-owned DEVICE memory on the current CUDA device, unless a
+ *     comment says otherwise. Tensors are contiguous and row-major, in the shapes given.
+ *     bf16 tensors are passed as uint16_t bit patterns.
+ *   - Every pointer must be 16-byte aligned (vector loads and TMA), or the call returns
+ *     DFLASH_INVALID_ARGUMENT.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream). They
+ *     allocate no device memory and do not synchronise the device. A non-OK status
+ *     means nothing was launched, except DFLASH_CUDA_ERROR, which reports a launch
+ *     failure.
+ *   - Supported sizes: R, S >= 1; 1 <= K <= 32 and K <= V; V < 2^31; H a multiple of 8;
+ *     rank a multiple of 8 in [8, 256]. Out-of-range sizes give DFLASH_INVALID_ARGUMENT
+ *     (bad values) or DFLASH_UNSUPPORTED (valid but not implemented, for example K > 32).
+ *   - Token ids are int32. Anchor ids outside [0, V) are caller errors. The kernels
+ *     check every gathered id: a bad id never reaches memory, its scores are NaN, and
+ *     the device status word records DFLASH_DEVICE_BAD_ID (see dflash_device_status).
+ *   - Calls that overlap on the GPU must not share an output or a workspace.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st* dflash_stream_t;
+
+typedef enum {
+    DFLASH_OK = 0,
+    DFLASH_INVALID_ARGUMENT = 1,    /* null or misaligned pointer, size out of range      */
+    DFLASH_UNSUPPORTED = 2,         /* valid request outside the implemented envelope     */
+    DFLASH_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the *_workspace_bytes query  */
+    DFLASH_CUDA_ERROR = 4,          /* a CUDA runtime call or a launch failed             */
+    DFLASH_NO_DEVICE = 5            /* no usable sm_100-family device is current          */
+} dflash_status;
+
+/* Bits of the device status word (dflash_device_status). */
+#define DFLASH_DEVICE_BAD_ID 0x1u       /* a gathered token id was outside [0, V)        */
+#define DFLASH_DEVICE_TIMEOUT 0x2u      /* a bounded wait inside a kernel gave up        */
+
+/* A static string naming a status code. Never NULL. */
+const char* dflash_status_string(int status);
+
+/* A detail message for the last non-OK status returned on this host thread ("" if none).
+ * The pointer stays valid until the next library call on this thread. */
+const char* dflash_last_error(void);
+
+/* ------------------------------------------------------------------------------------
+ * Step 1: top-K candidates.
+ * Source: DFlash2BeamForCausalLM.compute_candidates ("the selector's top-k candidate
+ * ids and their logits at each position").
+ *
+ * logits    [R, S, V] float32   the drafter's vocabulary logits, one row per (r, p)
+ * cand_ids  [R, S, K] int32     out: the K best token ids of each row, in candidate order
+ * unary     [R, S, K] float32   out: their logits
+ * workspace                     caller-owned device scratch of at least
+ *                               dflash_topk_workspace_bytes(R, S, V, K) bytes. Its
+ *                               contents on entry do not matter. The call overwrites it.
+ *
+ * Candidate order: logit descending; equal logits go to the lower token id; -0 equals
+ * +0. A NaN with the sign bit clear ranks above +inf, and one with the sign set below
+ * -inf. The unary value of a -0 logit is returned as +0.
+ * ---------------------------------------------------------------------------------- */
+size_t dflash_topk_workspace_bytes(int R, int S, int V, int K);
+
+dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, int K,
+                                     int32_t* cand_ids, float* unary, void* workspace,
+                                     size_t workspace_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Step 2: hidden projection, h = hidden . W_proj^T with no bias.
+ * Source: DFlash2BeamCandidateSelector.__init__ (hidden_projection: a bias-free linear
+ * map hidden_size -> rank, in params_dtype) and forward (hidden must be bf16).
+ *
+ * hidden  [R, S, H]    bf16   drafter hidden states
+ * w_proj  [rank, H]    bf16   projection weight, in the Linear [out, in] convention
+ * h_out   [R, S, rank] bf16   out: fp32 accumulation, rounded to bf16 (nearest-even)
+ * Runs on the tensor cores (tcgen05, operands staged by TMA). Needs an sm_100-family GPU.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_hidden_projection(const uint16_t* hidden, const uint16_t* w_proj,
+                                       int R, int S, int H, int rank, uint16_t* h_out,
+                                       dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Step 3: edge scores.
+ * Source: DFlash2BeamCandidateSelector (class docstring and forward): "[requests,
+ * steps, top_k (predecessor), top_k]".
+ *
+ * pred_cb, succ_cb  [V, rank]     bf16    predecessor / successor codebooks
+ * cand_ids          [R, S, K]     int32   candidates (step 1's output)
+ * unary             [R, S, K]     float32 their logits
+ * h                 [R, S, rank]  bf16    projected hidden states (step 2's output)
+ * anchors           [R]           int32   anchor (bonus) token of each request
+ * edges             [R, S, K, K]  float32 out: E[r, p, q, c], with q the predecessor
+ *                                         index and c the candidate index
+ *
+ * E[r,p,q,c] = unary[r,p,c] + sum_j pred_cb[pid, j] * h[r,p,j] * succ_cb[cand[r,p,c], j],
+ * with pid = cand[r,p-1,q] for p > 0 and pid = anchors[r] (every q) for p = 0. The
+ * products and sums are taken in fp32.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* succ_cb,
+                                     const int32_t* cand_ids, const float* unary,
+                                     const uint16_t* h, const int32_t* anchors, int R, int S,
+                                     int K, int V, int rank, float* edges,
+                                     dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * The whole selector in one call: step 2, then step 1, then step 3, all on `stream`
+ * with no host round trip. The outputs and workspace are as in the three calls above.
+ * Source: the draft step captures the candidate head and the selector together
+ * (module docstring of the page).
+ * ---------------------------------------------------------------------------------- */
+size_t dflash_selector_workspace_bytes(int R, int S, int V, int K);
+
+dflash_status dflash_selector(const float* logits, const uint16_t* hidden,
+                              const uint16_t* w_proj, const uint16_t* pred_cb,
+                              const uint16_t* succ_cb, const int32_t* anchors, int R, int S,
+                              int K, int V, int H, int rank, int32_t* cand_ids, float* unary,
+                              uint16_t* h_out, float* edges, void* workspace,
+                              size_t workspace_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Device status word. Reads the DFLASH_DEVICE_* bits that kernels on the current device
+ * have set since the last clear. Clears them if `clear` is non-zero. Synchronises the
+ * device. `flags` is a host pointer.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_device_status(uint32_t* flags, int clear);
+
+/* ------------------------------------------------------------------------------------
+ * Stage tracing for dflash_selector. There is no counterpart on the pages; this is a
+ * profiling aid.
+ * dflash_trace_begin(n) creates 4 timing events for each of the next n selector calls
+ * made from this process on the current device. Each traced call records them on its
+ * stream: before the projection, before the top-k, before the edges, after the edges.
+ * dflash_trace_end waits for the events. It writes up to max_calls rows of 3 stage
+ * times (ms: projection, top-k, edges) into `stage_ms` (a host array of 3 * max_calls
+ * floats), stores the row count in *n_calls, then releases the events.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_trace_begin(int n_calls);
+dflash_status dflash_trace_end(float* stage_ms, int max_calls, int* n_calls);
+
+/* Library version, "major.minor.patch". */
+const char* dflash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

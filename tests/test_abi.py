@@ -1,0 +1,105 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every function
+include/dflash.h declares, and rejects bad arguments before any CUDA call."""
+
+import ctypes
+
+import pytest
+import torch
+
+from draft_candidate_selector_gb300 import _native
+
+P = ctypes.c_void_p
+A = P(4096)     # a non-null, 16-byte aligned stand-in pointer (never dereferenced)
+MIS = P(4100)   # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _native.load()
+
+
+def test_header_symbols_exported(lib):
+    names = _native.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/dflash.h but not exported"
+    assert set(names) == set(_native.SIGNATURES), "binding signatures out of sync with header"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "DFLASH_OK"), (1, "DFLASH_INVALID_ARGUMENT"),
+                       (2, "DFLASH_UNSUPPORTED"), (3, "DFLASH_WORKSPACE_TOO_SMALL"),
+                       (4, "DFLASH_CUDA_ERROR"), (5, "DFLASH_NO_DEVICE"),
+                       (99, "DFLASH_UNKNOWN_STATUS")]:
+        assert lib.dflash_status_string(code).decode() == name
+    assert lib.dflash_version().decode().count(".") == 2
+
+
+def _topk(lib, R=2, S=3, V=100, K=4, logits=A, ids=A, un=A, ws=A, wsb=1 << 20):
+    return lib.dflash_topk_candidates(logits, R, S, V, K, ids, un, ws, wsb, None)
+
+
+def test_topk_argument_checks(lib):
+    assert _topk(lib, R=0) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, V=0) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, K=0) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, K=101, V=100) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, K=33) == _native.DFLASH_UNSUPPORTED
+    assert _topk(lib, logits=P(None)) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, ids=MIS) == _native.DFLASH_INVALID_ARGUMENT
+    assert b"aligned" in lib.dflash_last_error()
+    assert _topk(lib, ws=P(None)) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_projection_argument_checks(lib):
+    f = lib.dflash_hidden_projection
+    assert f(A, A, 2, 3, 60, 16, A, None) == _native.DFLASH_UNSUPPORTED      # H % 8
+    assert f(A, A, 2, 3, 64, 12, A, None) == _native.DFLASH_UNSUPPORTED      # rank % 8
+    assert f(A, A, 2, 3, 64, 264, A, None) == _native.DFLASH_UNSUPPORTED     # rank > 256
+    assert f(A, A, 0, 3, 64, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(P(None), A, 2, 3, 64, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(A, A, 2, 3, 64, 16, MIS, None) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_edges_argument_checks(lib):
+    f = lib.dflash_candidate_edges
+    args = [A] * 6
+    assert f(*args, 2, 3, 0, 100, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(*args, 2, 3, 40, 100, 16, A, None) == _native.DFLASH_UNSUPPORTED
+    assert f(*args, 2, 3, 8, 4, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT   # K > V
+    assert f(*args, 2, 3, 8, 100, 20, A, None) == _native.DFLASH_UNSUPPORTED      # rank % 8
+    assert f(A, A, A, A, A, P(None), 2, 3, 8, 100, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_selector_argument_checks(lib):
+    f = lib.dflash_selector
+    good = dict(R=2, S=3, K=4, V=100, H=64, rank=16)
+
+    def call(**kw):
+        d = {**good, **kw}
+        ptrs = kw.pop("ptrs", [A] * 6)
+        return f(*ptrs, d["R"], d["S"], d["K"], d["V"], d["H"], d["rank"], A, A, A, A, A,
+                 1 << 20, None)
+
+    assert call(K=33) == _native.DFLASH_UNSUPPORTED
+    assert call(H=12) == _native.DFLASH_UNSUPPORTED
+    assert call(V=2, K=4) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(ptrs=[A, A, A, A, MIS, A]) == _native.DFLASH_INVALID_ARGUMENT
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks behaviour without a GPU")
+def test_no_device_is_reported(lib):
+    assert _topk(lib) == _native.DFLASH_NO_DEVICE
+    assert lib.dflash_topk_workspace_bytes(2, 3, 100, 4) == 0
+    flags = ctypes.c_uint32(0)
+    assert lib.dflash_device_status(ctypes.byref(flags), 0) == _native.DFLASH_NO_DEVICE
+    assert lib.dflash_trace_begin(4) == _native.DFLASH_NO_DEVICE
+
+
+def test_python_errors_map_to_exceptions(lib):
+    with pytest.raises(ValueError):
+        _native.check(_native.DFLASH_INVALID_ARGUMENT)
+    with pytest.raises(NotImplementedError):
+        _native.check(_native.DFLASH_UNSUPPORTED)
+    with pytest.raises(_native.DflashError):
+        _native.check(_native.DFLASH_CUDA_ERROR)

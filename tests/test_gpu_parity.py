@@ -1,0 +1,333 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the CPU oracle on
+the same seeded inputs.
+
+Small workloads are compared in full. The large ones (qwen_zipf, gemma_softcap,
+gemma_large) run at full size, in the launch configuration the benchmark times, and are
+compared on sampled rows or requests that the oracle computes one by one. Edge cases
+cover ragged sizes (V, H and rank not multiples of the tile sizes), exact ties, signed
+zeros, infinities, NaNs, sorted rows, K = 1, K = V, K = 32, step 0 only, and bad ids.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity as P
+import draft_candidate_selector_gb300 as ds
+from draft_candidate_selector_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny", "small_ties"]
+LARGE = ["qwen_zipf", "gemma_softcap", "gemma_large"]
+# Several tiles and warps, with every size ragged: V % 4 = 1, H % 64 = 8, rank % 16 = 8.
+RAGGED = wl.custom_workload(3, 7, 16, 50001, 328, 40)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    ds.dflash_device_status(clear=True)
+    return d
+
+
+_CACHE: dict = {}
+
+
+def host_inputs(name):
+    """Seeded inputs, keeping one large workload in memory at a time."""
+    key = name if isinstance(name, str) else name.name
+    if key not in _CACHE:
+        if key in LARGE:
+            for k in [k for k in _CACHE if k in LARGE]:
+                del _CACHE[k]
+        _CACHE[key] = wl.make_inputs(name, seed=0)
+    return _CACHE[key]
+
+
+def _status_clean():
+    assert ds.dflash_device_status(clear=True) == 0
+
+
+# ----------------------------------------------------------------------------- top-k
+
+@pytest.mark.parametrize("name", SMALL + ["ragged"])
+def test_topk_small_full(dev, name):
+    inp = host_inputs(RAGGED if name == "ragged" else name)
+    w = inp.workload
+    x = torch.from_numpy(inp.logits).to(dev)
+    ids, un = ds.dflash_topk_candidates(x, w.K)
+    ref_ids, ref_un = oracle.topk(inp.logits, w.K)
+    P.assert_ids_equal(ids.cpu().numpy(), ref_ids, f"{name} ids")
+    P.assert_close(un.cpu().numpy(), ref_un, f"{name} unary")
+    _status_clean()
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_topk_large_sampled(dev, name):
+    inp = host_inputs(name)
+    w = inp.workload
+    x = torch.from_numpy(inp.logits).to(dev)
+    ids, un = ds.dflash_topk_candidates(x, w.K)
+    rows = P.sample_rows(w.rows, 40, seed=1)
+    ref_ids, ref_un = P.oracle_topk_rows(inp.logits, w.K, rows)
+    got_ids = ids.reshape(w.rows, w.K)[torch.from_numpy(rows).to(dev)].cpu().numpy()
+    got_un = un.reshape(w.rows, w.K)[torch.from_numpy(rows).to(dev)].cpu().numpy()
+    P.assert_ids_equal(got_ids, ref_ids, f"{name} ids")
+    P.assert_close(got_un, ref_un, f"{name} unary")
+    # Properties that hold at any size, on every row: distinct ids in range, unary equal
+    # to the logit at the id, and non-increasing unary.
+    ids_all = ids.reshape(w.rows, w.K)
+    assert int(ids_all.min()) >= 0 and int(ids_all.max()) < w.V
+    srt = torch.sort(ids_all, dim=1).values
+    assert bool((srt[:, 1:] != srt[:, :-1]).all())
+    gathered = torch.gather(x.reshape(w.rows, w.V), 1, ids_all.long())
+    assert torch.equal(gathered, un.reshape(w.rows, w.K))
+    assert bool((un[..., 1:] <= un[..., :-1]).all())
+    del x
+    _status_clean()
+
+
+def _topk_case(dev, x: np.ndarray, K: int, what: str):
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dev)
+    ids, un = ds.dflash_topk_candidates(xt, K)
+    ref_ids, ref_un = oracle.topk(x, K)
+    P.assert_ids_equal(ids.cpu().numpy(), ref_ids, what)
+    P.assert_close(un.cpu().numpy(), ref_un, what)
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 4, 5, 31, 32, 33, 127, 129, 4095, 4097, 65537])
+def test_topk_ragged_vocab(dev, V):
+    rng = np.random.default_rng(V)
+    x = rng.integers(-3, 4, size=(2, 3, V)).astype(np.float32)      # heavy ties
+    x[x == 0] = np.where(rng.random(int((x == 0).sum())) < 0.5, -0.0, 0.0)
+    for K in sorted({1, min(V, 7), min(V, 32)}):
+        _topk_case(dev, x, K, f"V={V} K={K}")
+
+
+def test_topk_special_values(dev):
+    V = 9000
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((4, 5, V)).astype(np.float32)
+    x[0, 0, ::7] = np.inf
+    x[0, 1, ::5] = -np.inf
+    x[0, 1, 1::5] = np.nan
+    x[0, 2, 3::11] = np.copysign(np.float32(np.nan), np.float32(-1))
+    x[0, 3, :] = -np.inf                       # the whole row at -inf: ties on ids
+    x[0, 4, :] = np.copysign(np.float32(np.nan), np.float32(-1))
+    x[1, 0, :] = 0.0
+    x[1, 0, ::2] = -0.0                        # signed zeros only
+    x[1, 1, :] = np.arange(V, dtype=np.float32)          # ascending: every element enters
+    x[1, 2, :] = -np.arange(V, dtype=np.float32)         # descending
+    x[1, 3, :] = 1e-45                         # subnormals
+    x[2] = np.float32(1.5)                     # all equal
+    for K in (1, 8, 32):
+        _topk_case(dev, x, K, f"special K={K}")
+
+
+def test_topk_many_small_rows(dev):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((50, 40, 33)).astype(np.float32)   # 2000 rows, V % 4 = 1
+    _topk_case(dev, x, 32, "V=33 K=32")
+    y = rng.standard_normal((7, 13, 4099)).astype(np.float32)
+    _topk_case(dev, y, 17, "V=4099 K=17")
+
+
+def test_topk_k_equals_v(dev):
+    rng = np.random.default_rng(4)
+    x = rng.integers(-2, 3, size=(3, 4, 32)).astype(np.float32)
+    _topk_case(dev, x, 32, "K = V = 32")
+
+
+def test_topk_reuses_workspace(dev):
+    """Two calls in a row with one workspace: the arrival counters start from zero again."""
+    inp = host_inputs(RAGGED)
+    w = inp.workload
+    x = torch.from_numpy(inp.logits).to(dev)
+    nb = ds.dflash_topk_workspace_bytes(w.R, w.S, w.V, w.K)
+    ws = torch.full((nb,), 0xAB, dtype=torch.uint8, device=dev)   # garbage on entry
+    ref_ids, _ = oracle.topk(inp.logits, w.K)
+    for _ in range(3):
+        ids, _ = ds.dflash_topk_candidates(x, w.K, workspace=ws)
+        P.assert_ids_equal(ids.cpu().numpy(), ref_ids, "reused workspace")
+
+
+# ----------------------------------------------------------------------------- projection
+
+def _projection_case(dev, rows, H, rank, seed, what):
+    g = torch.Generator().manual_seed(seed)
+    hid = torch.randn(1, rows, H, generator=g).to(torch.bfloat16)
+    w = (torch.randn(rank, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+    h = ds.dflash_hidden_projection(hid.to(dev), w.to(dev))
+    ref = oracle.projection(P.bits(hid), P.bits(w))
+    P.assert_bf16_within_one_step(P.bits(h), ref, what)
+
+
+@pytest.mark.parametrize("rows,H,rank", [
+    (1, 8, 8), (129, 72, 24), (300, 1000, 256), (256, 64, 128), (17, 4096, 40),
+    (1000, 5376, 256), (385, 3840, 128), (64, 2048, 136), (130, 520, 248),
+])
+def test_projection_shapes(dev, rows, H, rank):
+    _projection_case(dev, rows, H, rank, rows + H + rank, f"rows={rows} H={H} rank={rank}")
+    _status_clean()
+
+
+@pytest.mark.parametrize("name", SMALL + ["ragged"] + LARGE)
+def test_projection_workloads(dev, name):
+    inp = host_inputs(RAGGED if name == "ragged" else name)
+    w = inp.workload
+    h = ds.dflash_hidden_projection(inp.hidden.to(dev), inp.w_proj.to(dev))
+    if name in LARGE:
+        rows = P.sample_rows(w.rows, 64, seed=2, extra=range(120, 140))
+        hid = P.bits(inp.hidden).reshape(w.rows, w.H)[rows]
+        got = P.bits(h).reshape(w.rows, w.rank)[rows]
+    else:
+        hid = P.bits(inp.hidden)
+        got = P.bits(h)
+    ref = oracle.projection(hid, P.bits(inp.w_proj))
+    P.assert_bf16_within_one_step(got, ref, f"{name} h")
+    _status_clean()
+
+
+def test_projection_closed_forms(dev):
+    rows, H = 200, 256
+    g = torch.Generator().manual_seed(5)
+    hid = torch.randn(2, rows // 2, H, generator=g).to(torch.bfloat16).to(dev)
+    zero = torch.zeros(64, H, dtype=torch.bfloat16, device=dev)
+    assert torch.equal(ds.dflash_hidden_projection(hid, zero),
+                       torch.zeros(2, rows // 2, 64, dtype=torch.bfloat16, device=dev))
+    eye = torch.eye(H, dtype=torch.bfloat16, device=dev)       # rank = H = 256
+    assert torch.equal(ds.dflash_hidden_projection(hid, eye), hid)
+
+
+# ----------------------------------------------------------------------------- edges
+
+def _edge_inputs_from_oracle(inp: wl.Inputs, req: np.ndarray | None = None):
+    """Candidates, unary and h from the ORACLE, so the edge kernel is tested alone."""
+    w = inp.workload
+    logits = inp.logits if req is None else inp.logits[req]
+    hid = P.bits(inp.hidden) if req is None else P.bits(inp.hidden)[req]
+    anchors = inp.anchors if req is None else inp.anchors[req]
+    ids, un = oracle.topk(logits, w.K)
+    h = oracle.projection(hid, P.bits(inp.w_proj))
+    return ids, un, h, anchors
+
+
+def _run_edges(dev, inp, ids, un, h, anchors):
+    h_t = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev)
+    return ds.dflash_candidate_edges(
+        inp.pred_cb.to(dev), inp.succ_cb.to(dev), torch.from_numpy(ids).to(dev),
+        torch.from_numpy(un).to(dev), h_t, torch.from_numpy(anchors).to(dev))
+
+
+@pytest.mark.parametrize("name", SMALL + ["ragged"] + LARGE)
+def test_edges_workloads(dev, name):
+    inp = host_inputs(RAGGED if name == "ragged" else name)
+    req = P.sample_requests(inp.workload.R, 3, seed=3) if name in LARGE else None
+    ids, un, h, anchors = _edge_inputs_from_oracle(inp, req)
+    e = _run_edges(dev, inp, ids, un, h, anchors)
+    ref = oracle.edges(P.bits(inp.pred_cb), P.bits(inp.succ_cb), ids, un, h, anchors)
+    P.assert_close(e.cpu().numpy(), ref, f"{name} edges")
+    _status_clean()
+
+
+@pytest.mark.parametrize("R,S,K,V,rank", [
+    (2, 1, 4, 100, 16),      # step 0 only: every row from the anchor
+    (3, 5, 1, 50, 8),        # K = 1
+    (2, 4, 32, 64, 8),       # K = 32 with the smallest rank
+    (1, 3, 32, 40000, 256),  # K = 32, largest rank
+    (4, 6, 5, 77, 24),       # K not a power of two
+])
+def test_edges_shapes(dev, R, S, K, V, rank):
+    rng = np.random.default_rng(R * 1000 + K)
+    g = torch.Generator().manual_seed(K + rank)
+    pred = (torch.randn(V, rank, generator=g) / rank ** 0.5).to(torch.bfloat16)
+    succ = (torch.randn(V, rank, generator=g) / rank ** 0.5).to(torch.bfloat16)
+    ids = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(S)])
+                    for _ in range(R)]).astype(np.int32)
+    un = rng.standard_normal((R, S, K)).astype(np.float32)
+    h = P.bits(torch.randn(R, S, rank, generator=g).to(torch.bfloat16))
+    anchors = rng.integers(0, V, R).astype(np.int32)
+    e = ds.dflash_candidate_edges(
+        pred.to(dev), succ.to(dev), torch.from_numpy(ids).to(dev), torch.from_numpy(un).to(dev),
+        torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev),
+        torch.from_numpy(anchors).to(dev))
+    ref = oracle.edges(P.bits(pred), P.bits(succ), ids, un, h, anchors)
+    P.assert_close(e.cpu().numpy(), ref, f"edges R={R} S={S} K={K} V={V} rank={rank}")
+    # Structure that holds at any size: every predecessor row at step 0 is identical.
+    e0 = e[:, 0]
+    assert torch.equal(e0, e0[:, :1, :].expand_as(e0))
+    _status_clean()
+
+
+def test_edges_bad_ids_are_reported_not_followed(dev):
+    """An anchor or candidate id outside [0, V) gives NaN scores and sets the status bit."""
+    R, S, K, V, rank = 2, 3, 4, 50, 16
+    rng = np.random.default_rng(9)
+    g = torch.Generator().manual_seed(9)
+    pred = torch.randn(V, rank, generator=g).to(torch.bfloat16)
+    succ = torch.randn(V, rank, generator=g).to(torch.bfloat16)
+    ids = rng.integers(0, V, (R, S, K)).astype(np.int32)
+    ids[1, 2, 3] = V + 5          # bad candidate: column 3 of request 1, step 2
+    un = rng.standard_normal((R, S, K)).astype(np.float32)
+    h = P.bits(torch.randn(R, S, rank, generator=g).to(torch.bfloat16))
+    anchors = np.array([-1, 7], dtype=np.int32)   # bad anchor for request 0
+    e = ds.dflash_candidate_edges(
+        pred.to(dev), succ.to(dev), torch.from_numpy(ids).to(dev), torch.from_numpy(un).to(dev),
+        torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev),
+        torch.from_numpy(anchors).to(dev))
+    status = ds.dflash_device_status(clear=True)
+    assert status & ds.DEVICE_BAD_ID
+    ref = oracle.edges(P.bits(pred), P.bits(succ), ids, un, h, anchors, allow_bad_ids=True)
+    P.assert_close(e.cpu().numpy(), ref, "edges with bad ids")
+
+
+# ----------------------------------------------------------------------------- fused selector
+
+def _selector_check(dev, inp: wl.Inputs, req: np.ndarray | None, what: str):
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    ids, un, h, e = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                                       d["succ_cb"], d["anchors"], w.K)
+    sel = slice(None) if req is None else torch.from_numpy(req).to(dev)
+    logits = inp.logits if req is None else inp.logits[req]
+    hid = P.bits(inp.hidden) if req is None else P.bits(inp.hidden)[req]
+    anchors = inp.anchors if req is None else inp.anchors[req]
+    r_ids, r_un, r_h, r_e = oracle.selector(logits, hid, P.bits(inp.w_proj), P.bits(inp.pred_cb),
+                                            P.bits(inp.succ_cb), anchors, w.K)
+    P.assert_ids_equal(ids[sel].cpu().numpy(), r_ids, f"{what} ids")
+    P.assert_close(un[sel].cpu().numpy(), r_un, f"{what} unary")
+    P.assert_bf16_within_one_step(P.bits(h[sel]), r_h, f"{what} h")
+    P.assert_close(e[sel].cpu().numpy(), r_e, f"{what} edges")
+    del d
+    _status_clean()
+
+
+@pytest.mark.parametrize("name", SMALL + ["ragged"])
+def test_selector_small_full(dev, name):
+    _selector_check(dev, host_inputs(RAGGED if name == "ragged" else name), None, name)
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_selector_large_sampled(dev, name):
+    inp = host_inputs(name)
+    _selector_check(dev, inp, P.sample_requests(inp.workload.R, 2, seed=4), name)
+
+
+def test_selector_trace(dev):
+    inp = host_inputs("small_ties")
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    ds.dflash_trace_begin(3)
+    for _ in range(4):   # the fourth call is beyond the trace capacity and not traced
+        ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"], d["succ_cb"],
+                           d["anchors"], w.K)
+    stages = ds.dflash_trace_end(8)
+    assert len(stages) == 3
+    assert all(t >= 0 for row in stages for t in row) and all(row[1] > 0 for row in stages)
