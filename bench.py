@@ -85,10 +85,10 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback (6.8 TB/s, earlier GB300 measurement)"}
 
 
-def profiled_traffic(workload: str) -> float | None:
+def profiled_traffic(workload: wl.Workload) -> float | None:
     """DRAM bytes per top-k launch from the committed ncu summary, if it was taken on the
     current top-k source (its sha256 is recorded with it) and on this workload."""
-    if workload != "gemma_large" or not os.path.exists(PROFILE_TOPK):
+    if workload.name != "gemma_large" or workload.R != 512 or not os.path.exists(PROFILE_TOPK):
         return None
     with open(PROFILE_TOPK) as f:
         text = f.read()
@@ -321,7 +321,7 @@ def run_ours(args, w: wl.Workload) -> None:
         topk_bytes = b["logits"] + b["ids_unary_out"]
         peaks = measured_peaks()
         achieved = topk_bytes / (topk_ms / 1e3) / 1e9
-        traffic = profiled_traffic(w.name)
+        traffic = profiled_traffic(w)
         total_bytes = sum(b.values())
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -361,9 +361,15 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", default="gemma_large", choices=wl.WORKLOAD_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="override R (a smaller case of the same shape, e.g. for ncu captures)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
     w = wl.WORKLOADS[args.workload]
+    if args.requests is not None:
+        import dataclasses
+        w = dataclasses.replace(w, R=args.requests,
+                                description=f"{w.description}; R overridden to {args.requests}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
