@@ -21,6 +21,8 @@
 
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 namespace dflash {
 namespace {
 
@@ -155,11 +157,17 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
                          const uint16_t* succ_cb, const int32_t* cand_ids, const float* unary,
                          const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
                          int rank, float* edges, uint32_t* status_word, cudaStream_t stream) {
-    (void)dev;
     const size_t smem = (size_t)(K * rank + rank * 32) * sizeof(float) + 64 * sizeof(int);
-    cudaError_t err = cudaFuncSetAttribute(edges_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-    if (err != cudaSuccess) return err;
+    // The largest layout (K = 32, rank = 256) is allowed once per device; smaller ones fit.
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev.device], [&] {
+        const size_t max_smem = (size_t)(32 * 256 + 256 * 32) * sizeof(float) + 64 * sizeof(int);
+        attr_err[dev.device] = cudaFuncSetAttribute(
+            edges_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+    });
+    if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
     const long long rows = (long long)R * S;
     edges_kernel<<<(unsigned)rows, kThreads, smem, stream>>>(pred_cb, succ_cb, cand_ids, unary, h,
                                                              anchors, S, K, V, rank, edges,

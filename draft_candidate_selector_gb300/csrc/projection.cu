@@ -312,23 +312,32 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t smem_bytes(int BN) {
+    return 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * BK * 2) +
+           (2 * kStages + 1) * sizeof(uint64_t) + 16;
+}
+
 }  // namespace
 
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank, uint16_t* h_out,
                               uint32_t* status_word, cudaStream_t stream) {
-    (void)dev;
     const int BN = rank >= 128 ? 128 : ((rank + 15) / 16) * 16;
     const uint32_t tmem_cols = BN <= 32 ? 32u : (BN <= 64 ? 64u : 128u);
     CUtensorMap map_a, map_b;
     if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
         !encode_2d(&map_b, w_proj, (uint64_t)rank, (uint64_t)H, (uint32_t)BN))
         return cudaErrorInvalidValue;
-    const size_t smem = 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * BK * 2) +
-                        (2 * kStages + 1) * sizeof(uint64_t) + 16;
-    cudaError_t err = cudaFuncSetAttribute(projection_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
+    const size_t smem = smem_bytes(BN);
+    // Allow the largest layout (BN = 128) once per device; smaller tiles fit under it.
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev.device], [&] {
+        attr_err[dev.device] = cudaFuncSetAttribute(
+            projection_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(128));
+    });
+    if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
     dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((rank + BN - 1) / BN));
     projection_kernel<<<grid, kThreads, smem, stream>>>(map_a, map_b, h_out, M, rank, H, BN,
                                                         tmem_cols, status_word);
