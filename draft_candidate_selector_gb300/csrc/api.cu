@@ -208,6 +208,31 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
     return ok();
 }
 
+dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, int V, int K,
+                                             int32_t* cand_ids, float* unary,
+                                             dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_ptr(logits, "logits"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    dflash::DeviceInfo dev;
+    DFLASH_TRY(current_device(&dev, nullptr));
+    const dflash::TopkPlan plan = dflash::topk_plan(dev, (long long)R * S, V);
+    if (plan.workspace_bytes() > dflash::kStaticScratchBytes)
+        return fail(DFLASH_UNSUPPORTED,
+                    "R*S=%lld rows need %zu bytes of scratch; the built-in scratch holds %zu. "
+                    "Use dflash_topk_candidates with a caller-owned workspace",
+                    (long long)R * S, plan.workspace_bytes(), dflash::kStaticScratchBytes);
+    void* scratch = nullptr;
+    cudaError_t e = dflash::topk_static_scratch(dev.device, &scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(top-k scratch)");
+    // launch_topk clears the arrival counters on the stream before the kernel runs.
+    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, scratch,
+                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return ok();
+}
+
 dflash_status dflash_hidden_projection(const uint16_t* hidden, const uint16_t* w_proj, int R,
                                        int S, int H, int rank, uint16_t* h_out,
                                        dflash_stream_t stream) {

@@ -44,6 +44,13 @@ cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
                         int32_t* cand_ids, float* unary, void* workspace,
                         cudaStream_t stream);
 
+// Size of the fixed device array that dflash_topk_candidates_noalloc uses as its workspace.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+
+// Device address of that array on `device`, which must be the current device. The first
+// call per device looks it up (cudaGetSymbolAddress); later calls return the cached value.
+cudaError_t topk_static_scratch(int device, void** ptr);
+
 // ---------------------------------------------------------------- projection (projection.cu)
 
 // Returns cudaSuccess, or an error if the tensor maps cannot be encoded or the launch

@@ -269,7 +269,31 @@ int resident_blocks_per_sm(int device) {
     return cache[device];
 }
 
+// Scratch of dflash_topk_candidates_noalloc: a fixed array in device memory, loaded with
+// the library, so that callers which may not allocate device memory can still run the
+// top-k. It holds the per-row arrival counters and the warps' partial lists.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
 }  // namespace
+
+cudaError_t topk_static_scratch(int device, void** ptr) {
+    // Host code only sees a stand-in for the array's name, so its device address is looked
+    // up once per device, with that device current (the caller makes it current).
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    static cudaError_t err[64];
+    static bool done[64] = {false};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[device]) {
+        void* p = nullptr;
+        err[device] = cudaGetSymbolAddress(&p, g_static_scratch);
+        addr[device] = p;
+        done[device] = true;
+    }
+    *ptr = addr[device];
+    return err[device];
+}
 
 TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V) {
     TopkPlan p;

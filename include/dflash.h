@@ -86,6 +86,29 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
                                      size_t workspace_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * Top-K candidates without a workspace argument. The pages have no counterpart to this
+ * call; it exists for callers that must not allocate device memory. Examples are a
+ * plugin running inside an inference engine that has already claimed all device memory
+ * for its own pool, and code that may not call cudaMalloc because the allocation would
+ * synchronise the device or is forbidden at that point.
+ *
+ * Same inputs, outputs and results as dflash_topk_candidates. The scratch is a fixed
+ * 4 MiB array in device memory that the library holds on every GPU that loads it, until
+ * the process exits. A call whose scratch need (about R*S*4 bytes of counters plus
+ * 512 bytes per streaming warp) exceeds 4 MiB returns DFLASH_UNSUPPORTED and launches
+ * nothing; use dflash_topk_candidates with a workspace then.
+ * - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * - The first call on a device looks up the array's device address. Make that first call
+ *   before any stream capture on the device.
+ * - Every call on a device shares the one array. Each call clears the counters it needs
+ *   (a memset on `stream`) before its kernel runs. Calls that overlap on the GPU (on
+ *   different streams, or from several threads) race on the array: serialise them.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, int V, int K,
+                                             int32_t* cand_ids, float* unary,
+                                             dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Step 2: hidden projection, h = hidden . W_proj^T with no bias.
  * Source: DFlash2BeamCandidateSelector.__init__ (hidden_projection: a bias-free linear
  * map hidden_size -> rank, in params_dtype) and forward (hidden must be bf16).
