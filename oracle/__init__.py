@@ -29,14 +29,14 @@ class Oracle:
         i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         lib.oracle_bf16_round.argtypes = [ctypes.c_double]
         lib.oracle_bf16_round.restype = ctypes.c_uint16
-        lib.oracle_topk.argtypes = [p, i64, i64, i32, p, p, i32]
+        lib.oracle_topk.argtypes = [p, i64, i64, i32, ctypes.c_double, ctypes.c_double, p, p, i32]
         lib.oracle_topk.restype = i32
         lib.oracle_projection.argtypes = [p, p, i64, i64, i64, p, p, i32]
         lib.oracle_projection.restype = i32
         lib.oracle_edges.argtypes = [p, p, i64, i64, p, p, p, p, i64, i64, i32, p, i32]
         lib.oracle_edges.restype = i32
         lib.oracle_selector.argtypes = [p, p, p, p, p, p, i64, i64, i32, i64, i64, i64,
-                                        p, p, p, p, i32]
+                                        ctypes.c_double, ctypes.c_double, p, p, p, p, i32]
         lib.oracle_selector.restype = i32
         self.lib = lib
         self.path = path
@@ -45,11 +45,13 @@ class Oracle:
         """Bit pattern of the bf16 nearest to x (ties to even), rounded in one step."""
         return int(self.lib.oracle_bf16_round(float(x)))
 
-    def topk(self, logits: np.ndarray, K: int, threads: int | None = None):
+    def topk(self, logits: np.ndarray, K: int, threads: int | None = None,
+             softcap: float = 0.0, scale: float = 1.0):
         """Top-K of each row of logits[..., V]: ids int32 [..., K], unary float32 [..., K].
 
         The order is logit descending, then token id ascending (-0 == +0). A NaN with the
-        sign clear ranks above +inf, one with the sign set below -inf.
+        sign clear ranks above +inf, one with the sign set below -inf. unary is the
+        processed logit scale * softcap * tanh(x / softcap) (no cap if softcap <= 0).
         """
         x = _c(logits, np.float32)
         V = x.shape[-1]
@@ -57,8 +59,8 @@ class Oracle:
         rows = int(np.prod(lead)) if lead else 1
         ids = np.empty(lead + (K,), dtype=np.int32)
         unary = np.empty(lead + (K,), dtype=np.float32)
-        rc = self.lib.oracle_topk(_ptr(x), rows, V, K, _ptr(ids), _ptr(unary),
-                                  threads or default_threads())
+        rc = self.lib.oracle_topk(_ptr(x), rows, V, K, float(softcap), float(scale), _ptr(ids),
+                                  _ptr(unary), threads or default_threads())
         if rc != 0:
             raise ValueError(f"oracle_topk failed (rc={rc}) for V={V}, K={K}")
         return ids, unary
@@ -113,7 +115,7 @@ class Oracle:
 
     def selector(self, logits: np.ndarray, hidden_bits: np.ndarray, w_bits: np.ndarray,
                  pred_bits: np.ndarray, succ_bits: np.ndarray, anchors: np.ndarray, K: int,
-                 threads: int | None = None):
+                 threads: int | None = None, softcap: float = 0.0, scale: float = 1.0):
         """All three steps for logits [R, S, V]: returns (ids, unary, h_bits, edges)."""
         x = _c(logits, np.float32)
         R, S, V = x.shape
@@ -129,8 +131,9 @@ class Oracle:
         h = np.empty((R, S, rank), dtype=np.uint16)
         e = np.empty((R, S, K, K), dtype=np.float32)
         rc = self.lib.oracle_selector(_ptr(x), _ptr(hid), _ptr(w), _ptr(a), _ptr(b), _ptr(anc),
-                                      R, S, K, V, H, rank, _ptr(ids), _ptr(un), _ptr(h),
-                                      _ptr(e), threads or default_threads())
+                                      R, S, K, V, H, rank, float(softcap), float(scale),
+                                      _ptr(ids), _ptr(un), _ptr(h), _ptr(e),
+                                      threads or default_threads())
         if rc != 0:
             raise ValueError(f"oracle_selector failed (rc={rc})")
         return ids, un, h, e
@@ -163,8 +166,8 @@ def bf16_round(x: float) -> int:
     return get().bf16_round(x)
 
 
-def topk(logits, K, threads=None):
-    return get().topk(logits, K, threads)
+def topk(logits, K, threads=None, softcap=0.0, scale=1.0):
+    return get().topk(logits, K, threads, softcap, scale)
 
 
 def projection(hidden_bits, w_bits, threads=None, want_exact=False):
@@ -177,9 +180,10 @@ def edges(pred_bits, succ_bits, cand, unary, h_bits, anchors, threads=None,
                        allow_bad_ids)
 
 
-def selector(logits, hidden_bits, w_bits, pred_bits, succ_bits, anchors, K, threads=None):
+def selector(logits, hidden_bits, w_bits, pred_bits, succ_bits, anchors, K, threads=None,
+             softcap=0.0, scale=1.0):
     return get().selector(logits, hidden_bits, w_bits, pred_bits, succ_bits, anchors, K,
-                          threads)
+                          threads, softcap, scale)
 
 
 def bits_to_float(bits: np.ndarray) -> np.ndarray:

@@ -23,7 +23,11 @@
  *   - Top-k order: logit descending; equal logits go to the lower token id; -0 and +0
  *     are equal. A NaN with the sign bit clear ranks above +inf, and one with the sign
  *     bit set ranks below -inf. NaNs of one sign are equal to each other.
- *   - unary = the selected logit itself, in fp32.
+ *   - unary = the selected logit itself, in fp32. With the logits processor's options
+ *     (DFlash2BeamForCausalLM.__init__ on the second page: LogitsProcessor(soft_cap,
+ *     scale=output_multiplier)), unary = scale * cap * tanh(x / cap), the cap applied
+ *     first. The selection and order still use the raw logits: the map is strictly
+ *     increasing for scale > 0.
  *   - Projection: an exact (fp64) dot product, rounded once to bf16, nearest-even.
  *   - Edges: exact (fp64) sums over the bf16 values, stored as fp32. pred*h is not
  *     rounded before the dot product.
@@ -137,10 +141,19 @@ typedef struct {
     const float* logits;
     int64_t V;
     int K;
+    double softcap;   /* <= 0: no cap */
+    double scale;
     int32_t* ids;
     float* unary;
     int failed;
 } topk_ctx;
+
+/* The logits processor applied to one selected logit: cap * tanh(x / cap), then * scale. */
+static float processed_logit(float x, double softcap, double scale) {
+    double v = (double)x;
+    if (softcap > 0.0) v = softcap * tanh(v / softcap);
+    return (float)(v * scale);
+}
 
 static void topk_row(void* vctx, int64_t r) {
     topk_ctx* c = (topk_ctx*)vctx;
@@ -157,18 +170,19 @@ static void topk_row(void* vctx, int64_t r) {
     qsort(e, (size_t)c->V, sizeof(entry_t), entry_order);
     for (int k = 0; k < c->K; ++k) {
         c->ids[r * c->K + k] = e[k].id;
-        c->unary[r * c->K + k] = e[k].v;
+        c->unary[r * c->K + k] = processed_logit(e[k].v, c->softcap, c->scale);
     }
     free(e);
 }
 
 /* For each of `rows` rows of `V` logits: the K first tokens of the candidate order
- * (logit descending, then token id ascending) and their logits.
- * Returns 0, or -1 on bad arguments or allocation failure. */
-int oracle_topk(const float* logits, int64_t rows, int64_t V, int K, int32_t* ids,
-                float* unary, int threads) {
+ * (logit descending, then token id ascending) and their processed logits (softcap <= 0
+ * and scale = 1 leave them raw). Returns 0, or -1 on bad arguments or allocation failure. */
+int oracle_topk(const float* logits, int64_t rows, int64_t V, int K, double softcap,
+                double scale, int32_t* ids, float* unary, int threads) {
     if (!logits || !ids || !unary || rows < 0 || V < 1 || K < 1 || K > V) return -1;
-    topk_ctx c = {logits, V, K, ids, unary, 0};
+    if (!(scale > 0.0)) return -1;
+    topk_ctx c = {logits, V, K, softcap, scale, ids, unary, 0};
     parallel_rows(topk_row, &c, rows, threads);
     return c.failed ? -1 : 0;
 }
@@ -267,12 +281,14 @@ int oracle_edges(const uint16_t* pred_cb, const uint16_t* succ_cb, int64_t V, in
 
 /* ---------------------------------------------------------------- all three steps */
 
-/* The whole selector for R requests: top-k, projection, edges. Outputs as above. */
+/* The whole selector for R requests: top-k (with the processed unary), projection, edges.
+ * Outputs as above; the edge scores use the processed unary values. */
 int oracle_selector(const float* logits, const uint16_t* hidden, const uint16_t* w,
                     const uint16_t* pred_cb, const uint16_t* succ_cb, const int32_t* anchors,
                     int64_t R, int64_t S, int K, int64_t V, int64_t H, int64_t rank,
-                    int32_t* ids, float* unary, uint16_t* h_out, float* edges, int threads) {
-    int rc = oracle_topk(logits, R * S, V, K, ids, unary, threads);
+                    double softcap, double scale, int32_t* ids, float* unary, uint16_t* h_out,
+                    float* edges, int threads) {
+    int rc = oracle_topk(logits, R * S, V, K, softcap, scale, ids, unary, threads);
     if (rc) return rc;
     rc = oracle_projection(hidden, w, R * S, H, rank, h_out, NULL, threads);
     if (rc) return rc;

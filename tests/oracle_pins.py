@@ -161,6 +161,30 @@ def pin_topk_invariants(orc, seed: int = 3) -> None:
             assert all(_sort_key(float(x[r][i]), int(i)) > kth for i in rest)
 
 
+def pin_topk_logits_processor_golden(orc) -> None:
+    for line in _golden_lines("logits_processor.txt"):
+        head, logits_s, ids_s, un_s = [p.strip() for p in line.split(";")]
+        cap, scale, K = head.split()
+        x = np.array([_parse_float(t) for t in logits_s.split()], dtype=np.float32)
+        ids, unary = orc.topk(x[None, :], int(K), softcap=float(cap), scale=float(scale))
+        assert ids[0].tolist() == [int(t) for t in ids_s.split()], (line, ids[0].tolist())
+        want = np.array([float(t) for t in un_s.split()], dtype=np.float32)
+        assert np.allclose(unary[0], want, rtol=1e-6, atol=0), (line, unary[0], want)
+
+
+def pin_topk_logits_processor_vs_numpy(orc, seed: int = 13) -> None:
+    """Against numpy's tanh: unary = float32(scale * cap * tanh(x / cap)), ids unchanged."""
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((6, 3000)) * 40).astype(np.float32)
+    ids_raw, un_raw = orc.topk(x, 16)
+    for cap, scale in ((30.0, 1.0), (10.0, 0.25), (0.0, 2.0), (50.0, 3.0)):
+        ids, un = orc.topk(x, 16, softcap=cap, scale=scale)
+        assert np.array_equal(ids, ids_raw)
+        v = un_raw.astype(np.float64)
+        want = (cap * np.tanh(v / cap) if cap > 0 else v) * scale
+        assert np.allclose(un, want.astype(np.float32), rtol=2e-7, atol=1e-30)
+
+
 # ----------------------------------------------------------------------------- bf16 rounding
 
 def pin_bf16_round_cases(orc) -> None:
@@ -369,8 +393,8 @@ def pin_selector_composes(orc, seed: int = 12) -> None:
     hid, w = bits(torch.randn(R, S, H, generator=g)), bits(torch.randn(rank, H, generator=g) / 6)
     a, b = bits(torch.randn(V, rank, generator=g) / 3), bits(torch.randn(V, rank, generator=g) / 3)
     anc = rng.integers(0, V, R).astype(np.int32)
-    ids, un, h, e = orc.selector(logits, hid, w, a, b, anc, K)
-    ids2, un2 = orc.topk(logits, K)
+    ids, un, h, e = orc.selector(logits, hid, w, a, b, anc, K, softcap=3.0, scale=0.5)
+    ids2, un2 = orc.topk(logits, K, softcap=3.0, scale=0.5)
     h2 = orc.projection(hid, w)
     e2 = orc.edges(a, b, ids2, un2, h2, anc)
     assert np.array_equal(ids, ids2) and np.array_equal(un, un2)
@@ -379,6 +403,7 @@ def pin_selector_composes(orc, seed: int = 12) -> None:
 
 ALL_PINS = [
     pin_topk_golden, pin_topk_bruteforce, pin_topk_stable_sort, pin_topk_invariants,
+    pin_topk_logits_processor_golden, pin_topk_logits_processor_vs_numpy,
     pin_bf16_round_cases, pin_bf16_round_vs_torch, pin_bf16_round_nearest,
     pin_projection_golden, pin_projection_closed_forms, pin_projection_vs_numpy,
     pin_edges_golden, pin_edges_zero_codebooks, pin_edges_rank1, pin_edges_structure,

@@ -32,8 +32,17 @@ MUTANTS = [
      "if (isnan(v)) return signbit(v) ? 0 : 2;",
      "if (isnan(v)) return signbit(v) ? 2 : 0;"),
     ("unary_from_position_not_id",
-     "c->unary[r * c->K + k] = e[k].v;",
-     "c->unary[r * c->K + k] = row[k];"),
+     "processed_logit(e[k].v, c->softcap, c->scale);",
+     "processed_logit(row[k], c->softcap, c->scale);"),
+    ("processor_scale_before_cap",
+     "if (softcap > 0.0) v = softcap * tanh(v / softcap);\n    return (float)(v * scale);",
+     "v *= scale;\n    if (softcap > 0.0) v = softcap * tanh(v / softcap);\n    return (float)v;"),
+    ("processor_cap_ignored",
+     "if (softcap > 0.0) v = softcap * tanh(v / softcap);",
+     "(void)softcap;"),
+    ("processor_not_applied",
+     "c->unary[r * c->K + k] = processed_logit(e[k].v, c->softcap, c->scale);",
+     "c->unary[r * c->K + k] = e[k].v;"),
     ("projection_weight_transposed",
      "s += bf16_to_double(wj[i]) * bf16_to_double(x[i]);",
      "s += bf16_to_double(c->w[i * c->rank + j]) * bf16_to_double(x[i]); (void)wj;"),
