@@ -76,8 +76,13 @@ def _workspace(nbytes: int, dev: torch.device, workspace: torch.Tensor | None) -
 
 def dflash_topk_candidates(logits: torch.Tensor, K: int, cand_ids: torch.Tensor | None = None,
                            unary: torch.Tensor | None = None,
-                           workspace: torch.Tensor | None = None, stream=None):
-    """Top-K candidate ids (int32) and their logits (fp32) of logits [R, S, V] fp32."""
+                           workspace: torch.Tensor | None = None, stream=None,
+                           softcap: float = 0.0, scale: float = 1.0):
+    """Top-K candidate ids (int32) and their logits (fp32) of logits [R, S, V] fp32.
+
+    softcap and scale are the logits processor's options: the reported values are
+    scale * softcap * tanh(x / softcap) (no cap when softcap is 0).
+    """
     lib = _native.load()
     if logits.dim() != 3:
         raise ValueError("logits must be [R, S, V]")
@@ -93,8 +98,8 @@ def dflash_topk_candidates(logits: torch.Tensor, K: int, cand_ids: torch.Tensor 
         _need(unary, "unary", torch.float32, (R, S, K))
         ws = _workspace(lib.dflash_topk_workspace_bytes(R, S, V, K), dev, workspace)
         _native.check(lib.dflash_topk_candidates(
-            _ptr(logits), R, S, V, K, _ptr(cand_ids), _ptr(unary), _ptr(ws), ws.numel(),
-            _stream(dev, stream)))
+            _ptr(logits), R, S, V, K, float(softcap), float(scale), _ptr(cand_ids), _ptr(unary),
+            _ptr(ws), ws.numel(), _stream(dev, stream)))
     return cand_ids, unary
 
 
@@ -150,8 +155,11 @@ def dflash_selector(logits: torch.Tensor, hidden: torch.Tensor, w_proj: torch.Te
                     K: int, cand_ids: torch.Tensor | None = None,
                     unary: torch.Tensor | None = None, h_out: torch.Tensor | None = None,
                     edges: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                    stream=None):
-    """The whole selector in one library call: returns (cand_ids, unary, h, edges)."""
+                    stream=None, softcap: float = 0.0, scale: float = 1.0):
+    """The whole selector in one library call: returns (cand_ids, unary, h, edges).
+
+    softcap and scale are the logits processor's options (see dflash_topk_candidates).
+    """
     lib = _native.load()
     if logits.dim() != 3 or hidden.dim() != 3:
         raise ValueError("logits must be [R, S, V] and hidden [R, S, H]")
@@ -181,8 +189,8 @@ def dflash_selector(logits: torch.Tensor, hidden: torch.Tensor, w_proj: torch.Te
         ws = _workspace(lib.dflash_selector_workspace_bytes(R, S, V, K), dev, workspace)
         _native.check(lib.dflash_selector(
             _ptr(logits), _ptr(hidden), _ptr(w_proj), _ptr(pred_cb), _ptr(succ_cb),
-            _ptr(anchors), R, S, K, V, H, rank, _ptr(cand_ids), _ptr(unary), _ptr(h_out),
-            _ptr(edges), _ptr(ws), ws.numel(), _stream(dev, stream)))
+            _ptr(anchors), R, S, K, V, H, rank, float(softcap), float(scale), _ptr(cand_ids),
+            _ptr(unary), _ptr(h_out), _ptr(edges), _ptr(ws), ws.numel(), _stream(dev, stream)))
     return cand_ids, unary, h_out, edges
 
 

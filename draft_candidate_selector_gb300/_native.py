@@ -24,7 +24,7 @@ DEVICE_TIMEOUT = 0x2
 
 HEADER = os.path.join(_build.ROOT, "include", "dflash.h")
 
-_p, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_p, _i, _sz, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
 
 # name -> (restype, argtypes)
 SIGNATURES = {
@@ -33,12 +33,12 @@ SIGNATURES = {
     "dflash_last_error": (ctypes.c_char_p, []),
     "dflash_topk_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "dflash_selector_workspace_bytes": (_sz, [_i, _i, _i, _i]),
-    "dflash_topk_candidates": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _sz, _p]),
+    "dflash_topk_candidates": (_i, [_p, _i, _i, _i, _i, _f, _f, _p, _p, _p, _sz, _p]),
     "dflash_topk_candidates_noalloc": (_i, [_p, _i, _i, _i, _i, _p, _p, _p]),
     "dflash_hidden_projection": (_i, [_p, _p, _i, _i, _i, _i, _p, _p]),
     "dflash_candidate_edges": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
-    "dflash_selector": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p,
-                             _p, _sz, _p]),
+    "dflash_selector": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _f, _p, _p,
+                             _p, _p, _p, _sz, _p]),
     "dflash_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
     "dflash_trace_begin": (_i, [_i]),
     "dflash_trace_end": (_i, [ctypes.POINTER(ctypes.c_float), _i, ctypes.POINTER(ctypes.c_int)]),

@@ -6,6 +6,7 @@
 #include "dflash.h"
 #include "common.cuh"
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -126,6 +127,15 @@ dflash_status check_dims_edges(int R, int S, int K, int V, int rank) {
     return check_rank(rank);
 }
 
+dflash_status check_processor(float softcap, float scale) {
+    if (!(softcap >= 0.f) || isinf(softcap))
+        return fail(DFLASH_INVALID_ARGUMENT, "softcap=%g must be finite and >= 0 (0 = no cap)",
+                    (double)softcap);
+    if (!(scale > 0.f) || isinf(scale))
+        return fail(DFLASH_INVALID_ARGUMENT, "scale=%g must be finite and > 0", (double)scale);
+    return DFLASH_OK;
+}
+
 dflash_status check_ptr(const void* p, const char* name) {
     if (!p) return fail(DFLASH_INVALID_ARGUMENT, "%s is NULL", name);
     if (!aligned16(p)) return fail(DFLASH_INVALID_ARGUMENT, "%s is not 16-byte aligned", name);
@@ -189,9 +199,11 @@ size_t dflash_selector_workspace_bytes(int R, int S, int V, int K) {
 }
 
 dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, int K,
-                                     int32_t* cand_ids, float* unary, void* workspace,
-                                     size_t workspace_bytes, dflash_stream_t stream) {
+                                     float softcap, float scale, int32_t* cand_ids,
+                                     float* unary, void* workspace, size_t workspace_bytes,
+                                     dflash_stream_t stream) {
     DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_ptr(logits, "logits"));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
@@ -203,7 +215,7 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
         return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
                     workspace_bytes, plan.workspace_bytes());
     cudaError_t e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace,
-                                        reinterpret_cast<cudaStream_t>(stream));
+                                        reinterpret_cast<cudaStream_t>(stream), softcap, scale);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     return ok();
 }
@@ -275,9 +287,11 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
 dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const uint16_t* w_proj,
                               const uint16_t* pred_cb, const uint16_t* succ_cb,
                               const int32_t* anchors, int R, int S, int K, int V, int H, int rank,
-                              int32_t* cand_ids, float* unary, uint16_t* h_out, float* edges,
-                              void* workspace, size_t workspace_bytes, dflash_stream_t stream) {
+                              float softcap, float scale, int32_t* cand_ids, float* unary,
+                              uint16_t* h_out, float* edges, void* workspace,
+                              size_t workspace_bytes, dflash_stream_t stream) {
     DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
     DFLASH_TRY(check_ptr(logits, "logits"));
     DFLASH_TRY(check_ptr(hidden, "hidden"));
@@ -304,7 +318,7 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st);
+    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
     e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,

@@ -40,9 +40,10 @@ struct TopkPlan {
 
 TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V);
 
+// softcap > 0 and scale != 1 apply the logits processor to the reported unary values.
 cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
                         int32_t* cand_ids, float* unary, void* workspace,
-                        cudaStream_t stream);
+                        cudaStream_t stream, float softcap = 0.f, float scale = 1.f);
 
 // Size of the fixed device array that dflash_topk_candidates_noalloc uses as its workspace.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;

@@ -143,12 +143,21 @@ __device__ __forceinline__ uint64_t merge_lists(uint64_t a, uint64_t b, int lane
     return m;
 }
 
+// The logits processor's options applied to a selected logit: scale * cap * tanh(x / cap),
+// or scale * x when cap == 0. Selection and order use the raw logits (the map is
+// increasing), so this touches only the K reported values.
+__device__ __forceinline__ float processed(float x, float softcap, float scale) {
+    if (softcap > 0.f) x = softcap * tanhf(x / softcap);
+    return x * scale;
+}
+
 __device__ __forceinline__ void write_row(uint64_t e, long long row, int lane, int K,
+                                          float softcap, float scale,
                                           int32_t* __restrict__ cand_ids,
                                           float* __restrict__ unary) {
     if (lane < K) {
         cand_ids[row * K + lane] = (int32_t)(~(uint32_t)e);
-        unary[row * K + lane] = key_value((uint32_t)(e >> 32));
+        unary[row * K + lane] = processed(key_value((uint32_t)(e >> 32)), softcap, scale);
     }
 }
 
@@ -205,8 +214,9 @@ __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict_
 
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const float* __restrict__ logits, long long total, long long span, int warps, int V,
-            int K, int32_t* __restrict__ cand_ids, float* __restrict__ unary,
-            uint32_t* __restrict__ counters, uint64_t* __restrict__ partials) {
+            int K, float softcap, float scale, int32_t* __restrict__ cand_ids,
+            float* __restrict__ unary, uint32_t* __restrict__ counters,
+            uint64_t* __restrict__ partials) {
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (gw >= warps) return;
@@ -227,7 +237,7 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
         const long long w0 = row_base / span;
         const long long w1 = (row_base + V - 1) / span;
         if (w0 == w1) {
-            write_row(L.e, r, lane, K, cand_ids, unary);
+            write_row(L.e, r, lane, K, softcap, scale, cand_ids, unary);
             continue;
         }
         // Only a warp's first and last rows can be shared: one slot for each.
@@ -248,7 +258,7 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
                 reinterpret_cast<const unsigned long long*>(partials) + (w * 2 + ws) * 32 + lane);
             m = merge_lists(m, other, lane);
         }
-        write_row(m, r, lane, K, cand_ids, unary);
+        write_row(m, r, lane, K, softcap, scale, cand_ids, unary);
     }
 }
 
@@ -313,14 +323,16 @@ TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V) {
 }
 
 cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
-                        int32_t* cand_ids, float* unary, void* workspace, cudaStream_t stream) {
+                        int32_t* cand_ids, float* unary, void* workspace, cudaStream_t stream,
+                        float softcap, float scale) {
     uint32_t* counters = static_cast<uint32_t*>(workspace);
     uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
                                                      plan.counter_bytes);
     cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
     if (err != cudaSuccess) return err;
     topk_kernel<<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span, plan.warps,
-                                                      V, K, cand_ids, unary, counters, partials);
+                                                      V, K, softcap, scale, cand_ids, unary,
+                                                      counters, partials);
     return cudaGetLastError();
 }
 

@@ -69,8 +69,15 @@ const char* dflash_last_error(void);
  * ids and their logits at each position").
  *
  * logits    [R, S, V] float32   the drafter's vocabulary logits, one row per (r, p)
+ * softcap, scale                the logits processor's options (second page,
+ *                               DFlash2BeamForCausalLM.__init__: LogitsProcessor(soft_cap,
+ *                               scale=output_multiplier)). The reported unary value is
+ *                               scale * softcap * tanh(x / softcap), the cap first; softcap = 0
+ *                               means no cap. scale must be > 0, so the map is increasing,
+ *                               and candidates are selected and ordered on the raw logits.
+ *                               Pass 0 and 1 for raw logits.
  * cand_ids  [R, S, K] int32     out: the K best token ids of each row, in candidate order
- * unary     [R, S, K] float32   out: their logits
+ * unary     [R, S, K] float32   out: their (processed) logits
  * workspace                     caller-owned device scratch of at least
  *                               dflash_topk_workspace_bytes(R, S, V, K) bytes. Its
  *                               contents on entry do not matter. The call overwrites it.
@@ -82,8 +89,9 @@ const char* dflash_last_error(void);
 size_t dflash_topk_workspace_bytes(int R, int S, int V, int K);
 
 dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, int K,
-                                     int32_t* cand_ids, float* unary, void* workspace,
-                                     size_t workspace_bytes, dflash_stream_t stream);
+                                     float softcap, float scale, int32_t* cand_ids,
+                                     float* unary, void* workspace, size_t workspace_bytes,
+                                     dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * Top-K candidates without a workspace argument. The pages have no counterpart to this
@@ -92,7 +100,8 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
  * for its own pool, and code that may not call cudaMalloc because the allocation would
  * synchronise the device or is forbidden at that point.
  *
- * Same inputs, outputs and results as dflash_topk_candidates. The scratch is a fixed
+ * Same inputs, outputs and results as dflash_topk_candidates with softcap = 0 and
+ * scale = 1 (raw logits). The scratch is a fixed
  * 4 MiB array in device memory that the library holds on every GPU that loads it, until
  * the process exits. A call whose scratch need (about R*S*4 bytes of counters plus
  * 512 bytes per streaming warp) exceeds 4 MiB returns DFLASH_UNSUPPORTED and launches
@@ -147,7 +156,8 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
 
 /* ------------------------------------------------------------------------------------
  * The whole selector in one call: step 2, then step 1, then step 3, all on `stream`
- * with no host round trip. The outputs and workspace are as in the three calls above.
+ * with no host round trip. The outputs, workspace, softcap and scale are as in the three
+ * calls above; the edge scores use the processed unary values.
  * Source: the draft step captures the candidate head and the selector together
  * (module docstring of the page).
  * ---------------------------------------------------------------------------------- */
@@ -156,9 +166,9 @@ size_t dflash_selector_workspace_bytes(int R, int S, int V, int K);
 dflash_status dflash_selector(const float* logits, const uint16_t* hidden,
                               const uint16_t* w_proj, const uint16_t* pred_cb,
                               const uint16_t* succ_cb, const int32_t* anchors, int R, int S,
-                              int K, int V, int H, int rank, int32_t* cand_ids, float* unary,
-                              uint16_t* h_out, float* edges, void* workspace,
-                              size_t workspace_bytes, dflash_stream_t stream);
+                              int K, int V, int H, int rank, float softcap, float scale,
+                              int32_t* cand_ids, float* unary, uint16_t* h_out, float* edges,
+                              void* workspace, size_t workspace_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * Device status word. Reads the DFLASH_DEVICE_* bits that kernels on the current device

@@ -35,8 +35,9 @@ def test_status_strings(lib):
     assert lib.dflash_version().decode().count(".") == 2
 
 
-def _topk(lib, R=2, S=3, V=100, K=4, logits=A, ids=A, un=A, ws=A, wsb=1 << 20):
-    return lib.dflash_topk_candidates(logits, R, S, V, K, ids, un, ws, wsb, None)
+def _topk(lib, R=2, S=3, V=100, K=4, logits=A, ids=A, un=A, ws=A, wsb=1 << 20, cap=0.0,
+          scale=1.0):
+    return lib.dflash_topk_candidates(logits, R, S, V, K, cap, scale, ids, un, ws, wsb, None)
 
 
 def test_topk_argument_checks(lib):
@@ -49,6 +50,10 @@ def test_topk_argument_checks(lib):
     assert _topk(lib, ids=MIS) == _native.DFLASH_INVALID_ARGUMENT
     assert b"aligned" in lib.dflash_last_error()
     assert _topk(lib, ws=P(None)) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, cap=-1.0) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, cap=float("inf")) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, scale=0.0) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, scale=float("nan")) == _native.DFLASH_INVALID_ARGUMENT
 
 
 def test_projection_argument_checks(lib):
@@ -78,13 +83,14 @@ def test_selector_argument_checks(lib):
     def call(**kw):
         d = {**good, **kw}
         ptrs = kw.pop("ptrs", [A] * 6)
-        return f(*ptrs, d["R"], d["S"], d["K"], d["V"], d["H"], d["rank"], A, A, A, A, A,
-                 1 << 20, None)
+        return f(*ptrs, d["R"], d["S"], d["K"], d["V"], d["H"], d["rank"], d.get("cap", 0.0),
+                 d.get("scale", 1.0), A, A, A, A, A, 1 << 20, None)
 
     assert call(K=33) == _native.DFLASH_UNSUPPORTED
     assert call(H=12) == _native.DFLASH_UNSUPPORTED
     assert call(V=2, K=4) == _native.DFLASH_INVALID_ARGUMENT
     assert call(ptrs=[A, A, A, A, MIS, A]) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(scale=-2.0) == _native.DFLASH_INVALID_ARGUMENT
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks behaviour without a GPU")

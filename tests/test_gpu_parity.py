@@ -371,3 +371,42 @@ def test_selector_cuda_graph_replay(dev):
                             f"graph replay {seed} h")
         P.assert_close(edges.cpu().numpy(), r_e, f"graph replay {seed} edges")
     _status_clean()
+
+
+# ----------------------------------------------------------------------------- logits processor
+
+@pytest.mark.parametrize("cap,scale", [(30.0, 1.0), (10.0, 0.5), (0.0, 2.0), (1.0, 1.0)])
+def test_topk_logits_processor(dev, cap, scale):
+    """Soft cap and output multiplier on the reported unary values; ids from raw logits."""
+    inp = host_inputs("small_ties")
+    w = inp.workload
+    x = inp.logits * np.float32(8.0)      # large logits, so tanh saturates in places
+    ids, un = ds.dflash_topk_candidates(torch.from_numpy(x).to(dev), w.K, softcap=cap,
+                                        scale=scale)
+    ref_ids, ref_un = oracle.topk(x, w.K, softcap=cap, scale=scale)
+    P.assert_ids_equal(ids.cpu().numpy(), ref_ids, f"cap={cap} scale={scale} ids")
+    P.assert_close(un.cpu().numpy(), ref_un, f"cap={cap} scale={scale} unary")
+
+
+def test_topk_logits_processor_saturation_keeps_raw_order(dev):
+    x = np.array([[[20.0, 30.0, -5.0, 25.0]]], dtype=np.float32)
+    ids, un = ds.dflash_topk_candidates(torch.from_numpy(x).to(dev), 3, softcap=1.0, scale=1.0)
+    assert ids.cpu().numpy().tolist() == [[[1, 3, 0]]]
+    assert un.cpu().numpy().tolist() == [[[1.0, 1.0, 1.0]]]
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_selector_logits_processor(dev, name):
+    inp = host_inputs(RAGGED if name == "ragged" else name)
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    ids, un, h, e = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                                       d["succ_cb"], d["anchors"], w.K, softcap=30.0, scale=1.5)
+    r_ids, r_un, r_h, r_e = oracle.selector(inp.logits, P.bits(inp.hidden), P.bits(inp.w_proj),
+                                            P.bits(inp.pred_cb), P.bits(inp.succ_cb),
+                                            inp.anchors, w.K, softcap=30.0, scale=1.5)
+    P.assert_ids_equal(ids.cpu().numpy(), r_ids, f"{name} ids")
+    P.assert_close(un.cpu().numpy(), r_un, f"{name} processed unary")
+    P.assert_projection(P.bits(h), P.bits(inp.hidden), P.bits(inp.w_proj), f"{name} h")
+    P.assert_close(e.cpu().numpy(), r_e, f"{name} edges")
+    _status_clean()
