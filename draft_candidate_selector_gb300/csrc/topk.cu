@@ -16,8 +16,10 @@
 //     complemented token id in the low word. Comparing two keys as integers gives the
 //     candidate order, ties included.
 //   * A float compare against the K-th entry's logit filters almost every element.
-//     It is conservative: NaNs and ties with the threshold value pass. Survivors are
-//     inserted one at a time, with a ballot for the position and a shuffle to shift.
+//     It is conservative: NaNs and ties with the threshold value pass. A few survivors
+//     are inserted one at a time, with a ballot for the position and a shuffle to shift.
+//     Many at once, as while the list fills at the start of a row, are sorted across the
+//     warp with a bitonic network and merged in one step.
 //   * A row split across warps: each warp writes its sorted list to the workspace and
 //     bumps the row's arrival counter. The warp that arrives last merges the lists with
 //     warp-wide bitonic merges and writes the row. Nobody waits, so nothing can hang.
@@ -32,7 +34,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
 constexpr int kUnroll = 8;              // 128-bit loads in flight per lane
-constexpr long long kMinSpan = 4096;    // smallest span given to one warp
+constexpr long long kMinSpan = 1024;    // smallest span given to one warp
 constexpr long long kSpanAlign = 128;   // spans start on 512-byte boundaries
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -106,9 +108,49 @@ __device__ __forceinline__ void list_insert(WarpList& L, uint64_t c, int lane, i
     L.thr_f = key_value((uint32_t)(L.thr >> 32));
 }
 
-// Offer every lane's candidate entry to the list, lowest lane first.
+// The 32 best of two sorted 32-lists: a bitonic merge across the warp.
+__device__ __forceinline__ uint64_t merge_lists(uint64_t a, uint64_t b, int lane) {
+    const uint64_t br = shfl64(b, 31 - lane);
+    uint64_t m = a > br ? a : br;             // bitonic, and holds the 32 best
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const uint64_t o = shfl_xor64(m, s);
+        const bool lower = (lane & s) == 0;
+        m = lower ? (m > o ? m : o) : (m < o ? m : o);
+    }
+    return m;
+}
+
+// Sort one entry per lane across the warp, best first (a bitonic sorting network).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = shfl_xor64(v, j);
+            const bool take_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = take_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    return v;
+}
+
+// Lanes with at least this many newcomers at once are merged as a sorted batch.
+constexpr int kBatchMergeMin = 6;
+
+// Offer every lane's candidate entry to the list. A few newcomers are inserted one at a
+// time, lowest lane first. Many at once (early in a row, when the list is still filling)
+// are sorted across the warp and merged in one step.
 __device__ __forceinline__ void list_offer(WarpList& L, uint64_t c, bool valid, int lane, int K) {
-    unsigned m = __ballot_sync(kFull, valid && c > L.thr);
+    const bool pass = valid && c > L.thr;
+    unsigned m = __ballot_sync(kFull, pass);
+    if (__popc(m) >= kBatchMergeMin) {
+        const uint64_t sorted = warp_sort_desc(pass ? c : 0ull, lane);
+        L.e = merge_lists(L.e, sorted, lane);
+        L.thr = shfl64(L.e, K - 1);
+        L.thr_f = key_value((uint32_t)(L.thr >> 32));
+        return;
+    }
     while (m) {
         const int src = __ffs(m) - 1;
         m &= m - 1;
@@ -128,19 +170,6 @@ __device__ __forceinline__ void offer4(WarpList& L, const float4& v, uint32_t co
     list_offer(L, make_entry(v.y, col + 1), valid, lane, K);
     list_offer(L, make_entry(v.z, col + 2), valid, lane, K);
     list_offer(L, make_entry(v.w, col + 3), valid, lane, K);
-}
-
-// The 32 best of two sorted 32-lists: a bitonic merge across the warp.
-__device__ __forceinline__ uint64_t merge_lists(uint64_t a, uint64_t b, int lane) {
-    const uint64_t br = shfl64(b, 31 - lane);
-    uint64_t m = a > br ? a : br;             // bitonic, and holds the 32 best
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const uint64_t o = shfl_xor64(m, s);
-        const bool lower = (lane & s) == 0;
-        m = lower ? (m > o ? m : o) : (m < o ? m : o);
-    }
-    return m;
 }
 
 // The logits processor's options applied to a selected logit: scale * cap * tanh(x / cap),
@@ -212,7 +241,7 @@ __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict_
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 topk_kernel(const float* __restrict__ logits, long long total, long long span, int warps, int V,
             int K, float softcap, float scale, int32_t* __restrict__ cand_ids,
             float* __restrict__ unary, uint32_t* __restrict__ counters,
