@@ -16,10 +16,12 @@
 //     complemented token id in the low word. Comparing two keys as integers gives the
 //     candidate order, ties included.
 //   * A float compare against the K-th entry's logit filters almost every element.
-//     It is conservative: NaNs and ties with the threshold value pass. A few survivors
-//     are inserted one at a time, with a ballot for the position and a shuffle to shift.
-//     Many at once, as while the list fills at the start of a row, are sorted across the
-//     warp with a bitonic network and merged in one step.
+//     It is conservative: NaNs and ties with the threshold value pass. Survivors are
+//     inserted one at a time, with a ballot for the position and a shuffle to shift.
+//   * The first group of a row is different: the list is empty, so everything would pass.
+//     Each lane takes the best of its own 32 values, the warp sorts those 32 lane-bests
+//     once, and they become the starting list. Its K-th entry is a valid threshold for
+//     the rest of the group, so only a handful of values go through the insert path.
 //   * A row split across warps: each warp writes its sorted list to the workspace and
 //     bumps the row's arrival counter. The warp that arrives last merges the lists with
 //     warp-wide bitonic merges and writes the row. Nobody waits, so nothing can hang.
@@ -33,7 +35,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarpsPerBlock = kThreads / 32;
-constexpr int kUnroll = 8;              // 128-bit loads in flight per lane
+constexpr int kUnroll = 8;              // 128-bit loads per lane per group (4 KB per warp)
+constexpr int kMinBlocks = 3;           // resident CTAs per SM the register budget targets
 constexpr long long kMinSpan = 1024;    // smallest span given to one warp
 constexpr long long kSpanAlign = 128;   // spans start on 512-byte boundaries
 constexpr unsigned kFull = 0xffffffffu;
@@ -121,7 +124,19 @@ __device__ __forceinline__ uint64_t merge_lists(uint64_t a, uint64_t b, int lane
     return m;
 }
 
-// Sort one entry per lane across the warp, best first (a bitonic sorting network).
+// Offer every lane's candidate entry to the list, lowest lane first.
+__device__ __forceinline__ void list_offer(WarpList& L, uint64_t c, bool valid, int lane, int K) {
+    unsigned m = __ballot_sync(kFull, valid && c > L.thr);
+    while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const uint64_t x = shfl64(c, src);
+        if (x > L.thr) list_insert(L, x, lane, K);
+    }
+}
+
+// Sort one entry per lane across the warp, best first (a bitonic sorting network). It runs
+// once per row segment, from one call site.
 __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
 #pragma unroll
     for (int k = 2; k <= 32; k <<= 1) {
@@ -133,30 +148,6 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
         }
     }
     return v;
-}
-
-// Lanes with at least this many newcomers at once are merged as a sorted batch.
-constexpr int kBatchMergeMin = 6;
-
-// Offer every lane's candidate entry to the list. A few newcomers are inserted one at a
-// time, lowest lane first. Many at once (early in a row, when the list is still filling)
-// are sorted across the warp and merged in one step.
-__device__ __forceinline__ void list_offer(WarpList& L, uint64_t c, bool valid, int lane, int K) {
-    const bool pass = valid && c > L.thr;
-    unsigned m = __ballot_sync(kFull, pass);
-    if (__popc(m) >= kBatchMergeMin) {
-        const uint64_t sorted = warp_sort_desc(pass ? c : 0ull, lane);
-        L.e = merge_lists(L.e, sorted, lane);
-        L.thr = shfl64(L.e, K - 1);
-        L.thr_f = key_value((uint32_t)(L.thr >> 32));
-        return;
-    }
-    while (m) {
-        const int src = __ffs(m) - 1;
-        m &= m - 1;
-        const uint64_t x = shfl64(c, src);
-        if (x > L.thr) list_insert(L, x, lane, K);
-    }
 }
 
 // Conservative float pre-filter: false only if all four values surely lose to t.
@@ -190,6 +181,64 @@ __device__ __forceinline__ void write_row(uint64_t e, long long row, int lane, i
     }
 }
 
+// First group of a row segment, with the list still empty. The lane-bests, sorted, start
+// the list: they are K or more real entries, so the K-th of them is a valid threshold.
+// The group is then read again (it is in L2 by now) and its other values are offered;
+// each lane's best is already in. Not holding the group in registers across the sort keeps
+// the kernel within its register budget.
+template <int U>
+__device__ __forceinline__ void first_group(WarpList& L, const float4* __restrict__ p,
+                                            uint32_t col0, int lane, int K) {
+    uint64_t best = 0;
+    int best_slot = -1;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const float4 v = ld_stream(p + u * 32 + lane);
+        const uint32_t col = col0 + (uint32_t)((u * 32 + lane) * 4);
+        uint64_t e = make_entry(v.x, col + 0);
+        if (e > best) { best = e; best_slot = u * 4 + 0; }
+        e = make_entry(v.y, col + 1);
+        if (e > best) { best = e; best_slot = u * 4 + 1; }
+        e = make_entry(v.z, col + 2);
+        if (e > best) { best = e; best_slot = u * 4 + 2; }
+        e = make_entry(v.w, col + 3);
+        if (e > best) { best = e; best_slot = u * 4 + 3; }
+    }
+    // Merge, not overwrite: an unaligned row head may already have put entries in the list.
+    L.e = merge_lists(L.e, warp_sort_desc(best, lane), lane);
+    L.thr = shfl64(L.e, K - 1);
+    L.thr_f = key_value((uint32_t)(L.thr >> 32));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const float4 v = ld_stream(p + u * 32 + lane);
+        if (__any_sync(kFull, may_enter(v, L.thr_f))) {
+            const uint32_t col = col0 + (uint32_t)((u * 32 + lane) * 4);
+            list_offer(L, make_entry(v.x, col + 0), best_slot != u * 4 + 0, lane, K);
+            list_offer(L, make_entry(v.y, col + 1), best_slot != u * 4 + 1, lane, K);
+            list_offer(L, make_entry(v.z, col + 2), best_slot != u * 4 + 2, lane, K);
+            list_offer(L, make_entry(v.w, col + 3), best_slot != u * 4 + 3, lane, K);
+        }
+    }
+}
+
+// Check one group of U float4 per lane (flat float4 index j + u*32 + lane) against the list.
+template <int U>
+__device__ __forceinline__ void check_group(WarpList& L, const float4 (&v)[U], uint32_t col0,
+                                            long long j, int lane, int K) {
+    bool hit = false;
+#pragma unroll
+    for (int u = 0; u < U; ++u) hit |= may_enter(v[u], L.thr_f);
+    if (__any_sync(kFull, hit)) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (__any_sync(kFull, may_enter(v[u], L.thr_f))) {
+                const uint32_t col = col0 + (uint32_t)((j + u * 32 + lane) * 4);
+                offer4(L, v[u], col, true, lane, K);
+            }
+        }
+    }
+}
+
 // Scan flat logits [lo, hi), all inside the row that starts at flat index row_base.
 __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict__ logits,
                                            long long lo, long long hi, long long row_base,
@@ -207,23 +256,17 @@ __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict_
     const long long n4 = (b4 - a4) >> 2;
     const uint32_t col0 = (uint32_t)(a4 - row_base);
 
+    constexpr long long kGroup = 32LL * kUnroll;     // float4s per group: 32 lines of 128 B
     long long j = 0;
-    for (; j + 32 * kUnroll <= n4; j += 32 * kUnroll) {
+    if (kGroup <= n4 && L.thr == 0) {                // a full first group, list still empty
+        first_group<kUnroll>(L, p, col0, lane, K);
+        j = kGroup;
+    }
+    for (; j + kGroup <= n4; j += kGroup) {
         float4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream(p + j + u * 32 + lane);
-        bool hit = false;
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) hit |= may_enter(v[u], L.thr_f);
-        if (__any_sync(kFull, hit)) {
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                if (__any_sync(kFull, may_enter(v[u], L.thr_f))) {
-                    const uint32_t col = col0 + (uint32_t)((j + u * 32 + lane) * 4);
-                    offer4(L, v[u], col, true, lane, K);
-                }
-            }
-        }
+        check_group<kUnroll>(L, v, col0, j, lane, K);
     }
     for (; j < n4; j += 32) {
         const long long idx = j + lane;
@@ -241,7 +284,7 @@ __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict_
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 topk_kernel(const float* __restrict__ logits, long long total, long long span, int warps, int V,
             int K, float softcap, float scale, int32_t* __restrict__ cand_ids,
             float* __restrict__ unary, uint32_t* __restrict__ counters,
