@@ -184,6 +184,15 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
         const int m0 = (item % m_tiles) * 16;
         const int n0 = (item / m_tiles) * 16;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // This lane's unary values, loaded before the contraction hides their latency.
+        float u[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int cc = n0 + nt * 8 + 2 * t + e;
+                u[nt][e] = cc < K ? un[cc] : 0.f;
+            }
         // A fragment words: rows m0+g and m0+g+8, columns k0+2t (+8).
         const uint32_t a_r0 = sbase + L.pred + (uint32_t)(m0 + g) * L.stride + 4u * t;
         const uint32_t a_r1 = a_r0 + 8u * L.stride;
@@ -192,6 +201,7 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
         const int mi = lane >> 3;
         const uint32_t b_ad = sbase + L.succ + (uint32_t)(n0 + (mi >> 1) * 8 + (lane & 7)) * L.stride +
                               (uint32_t)((mi & 1) * 16);
+#pragma unroll 4
         for (int k0 = 0; k0 < kpad; k0 += 16) {
             const uint32_t hw0 = lds32(h_w + 2 * k0), hw1 = lds32(h_w + 2 * k0 + 16);
             uint32_t hi0, hi1, hi2, hi3, lo0, lo1, lo2, lo3;
@@ -217,7 +227,7 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
                 for (int e = 0; e < 2; ++e) {
                     const int cc = c + e;
                     if (cc >= K) continue;
-                    float v = acc[nt][2 * half + e] + un[cc];
+                    float v = acc[nt][2 * half + e] + u[nt][e];
                     if (bad_q[q] || bad_c[cc]) v = __int_as_float(0x7FC00000);
                     out[q * K + cc] = v;
                 }
