@@ -47,6 +47,11 @@ struct DeviceSlot {
     dflash::DeviceInfo info;
     uint32_t* status_word = nullptr;
     bool ready = false;
+    // The fused selector runs the projection on this stream, beside the top-k.
+    std::mutex fork_mu;
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join = nullptr;
 };
 
 std::mutex g_dev_mu;
@@ -84,6 +89,20 @@ dflash_status current_device(dflash::DeviceInfo* info, uint32_t** status_word) {
     }
     if (info) *info = s.info;
     if (status_word) *status_word = s.status_word;
+    return DFLASH_OK;
+}
+
+// The side stream and fork/join events of the current device, created on first use.
+dflash_status side_stream(int device, DeviceSlot** slot) {
+    DeviceSlot& s = g_dev[device];
+    std::lock_guard<std::mutex> lock(s.fork_mu);
+    if (!s.side) {
+        cudaError_t e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "creating the selector's side stream");
+    }
+    *slot = &s;
     return DFLASH_OK;
 }
 
@@ -312,15 +331,26 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
         return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
                     workspace_bytes, plan.workspace_bytes());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    DeviceSlot* slot = nullptr;
+    DFLASH_TRY(side_stream(dev.device, &slot));
     cudaEvent_t* ev = trace_slot(dev.device);
+    // The projection does not depend on the top-k, and one projection CTA per SM fits
+    // beside the top-k's: fork it onto the side stream, join before the edges. The lock
+    // keeps the record/wait pairs of concurrent callers from interleaving.
+    std::lock_guard<std::mutex> lock(slot->fork_mu);
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st);
+    if ((e = cudaEventRecord(slot->fork, st)) != cudaSuccess) return cuda_fail(e, "fork event");
+    if ((e = cudaStreamWaitEvent(slot->side, slot->fork, 0)) != cudaSuccess)
+        return cuda_fail(e, "fork wait");
+    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, slot->side);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    if (ev && (e = cudaEventRecord(ev[1], slot->side)) != cudaSuccess) return cuda_fail(e, "trace event");
+    if ((e = cudaEventRecord(slot->join, slot->side)) != cudaSuccess) return cuda_fail(e, "join event");
     e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    if ((e = cudaStreamWaitEvent(st, slot->join, 0)) != cudaSuccess) return cuda_fail(e, "join wait");
     e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
                              rank, edges, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "edges launch");
@@ -374,9 +404,12 @@ dflash_status dflash_trace_end(float* stage_ms, int max_calls, int* n_calls) {
     for (int i = 0; i < n && st == DFLASH_OK; ++i) {
         cudaEvent_t* ev = &g_trace.events[4 * (size_t)i];
         cudaError_t e = cudaEventSynchronize(ev[3]);
+        // Events: [0] start, [1] projection done (side stream), [2] top-k done, [3] edges
+        // done. The projection and the top-k both start at [0] and run side by side.
+        const int from[3] = {0, 0, 2}, to[3] = {1, 2, 3};
         for (int k = 0; k < 3 && e == cudaSuccess; ++k) {
             float ms = 0.f;
-            e = cudaEventElapsedTime(&ms, ev[k], ev[k + 1]);
+            e = cudaEventElapsedTime(&ms, ev[from[k]], ev[to[k]]);
             if (stage_ms) stage_ms[3 * i + k] = ms;
         }
         if (e != cudaSuccess) st = cuda_fail(e, "reading trace events");

@@ -155,8 +155,11 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
                                      dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
- * The whole selector in one call: step 2, then step 1, then step 3, all on `stream`
- * with no host round trip. The outputs, workspace, softcap and scale are as in the three
+ * The whole selector in one call, with no host round trip. Step 2 (projection) runs on a
+ * library-owned side stream beside step 1 (top-k) on `stream`; step 3 (edges) follows
+ * both on `stream`. The call returns once everything is enqueued; later work on `stream`
+ * sees all outputs. It is safe to capture in a CUDA graph: the side stream joins the
+ * capture through an event. The outputs, workspace, softcap and scale are as in the three
  * calls above; the edge scores use the processed unary values.
  * Source: the draft step captures the candidate head and the selector together
  * (module docstring of the page).
@@ -181,11 +184,12 @@ dflash_status dflash_device_status(uint32_t* flags, int clear);
  * Stage tracing for dflash_selector. There is no counterpart on the pages; this is a
  * profiling aid.
  * dflash_trace_begin(n) creates 4 timing events for each of the next n selector calls
- * made from this process on the current device. Each traced call records them on its
- * stream: before the projection, before the top-k, before the edges, after the edges.
- * dflash_trace_end waits for the events. It writes up to max_calls rows of 3 stage
- * times (ms: projection, top-k, edges) into `stage_ms` (a host array of 3 * max_calls
- * floats), stores the row count in *n_calls, then releases the events.
+ * made from this process on the current device. Each traced call records them: at its
+ * start, when the projection is done (side stream), when the top-k is done and when the
+ * edges are done. dflash_trace_end waits for the events. It writes up to max_calls rows
+ * of 3 stage times (ms) into `stage_ms` (a host array of 3 * max_calls floats): the
+ * projection and the top-k, each from the start (they run side by side), and the edges.
+ * It stores the row count in *n_calls, then releases the events.
  * ---------------------------------------------------------------------------------- */
 dflash_status dflash_trace_begin(int n_calls);
 dflash_status dflash_trace_end(float* stage_ms, int max_calls, int* n_calls);
