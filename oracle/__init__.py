@@ -38,6 +38,9 @@ class Oracle:
         lib.oracle_selector.argtypes = [p, p, p, p, p, p, i64, i64, i32, i64, i64, i64,
                                         ctypes.c_double, ctypes.c_double, p, p, p, p, i32]
         lib.oracle_selector.restype = i32
+        lib.oracle_lmhead_topk.argtypes = [p, p, i64, i64, i64, i32, ctypes.c_double,
+                                           ctypes.c_double, p, p, p, i32]
+        lib.oracle_lmhead_topk.restype = i32
         self.lib = lib
         self.path = path
 
@@ -64,6 +67,32 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_topk failed (rc={rc}) for V={V}, K={K}")
         return ids, unary
+
+    def lmhead_topk(self, hidden_bits: np.ndarray, lm_head_bits: np.ndarray, K: int,
+                    threads: int | None = None, softcap: float = 0.0, scale: float = 1.0,
+                    want_logits: bool = False):
+        """Top-K of the exact logits hidden . lm_head^T (fp64): ids, processed unary values,
+        and, with want_logits, the exact logits [..., V] (float64).
+
+        hidden_bits uint16 [..., H]; lm_head_bits uint16 [V, H].
+        """
+        x = _c(hidden_bits, np.uint16)
+        w = _c(lm_head_bits, np.uint16)
+        H = x.shape[-1]
+        V = w.shape[0]
+        assert w.shape == (V, H)
+        lead = x.shape[:-1]
+        rows = int(np.prod(lead)) if lead else 1
+        ids = np.empty(lead + (K,), dtype=np.int32)
+        unary = np.empty(lead + (K,), dtype=np.float32)
+        logits = np.empty(lead + (V,), dtype=np.float64) if want_logits else None
+        rc = self.lib.oracle_lmhead_topk(_ptr(x), _ptr(w), rows, H, V, K, float(softcap),
+                                         float(scale), _ptr(ids), _ptr(unary),
+                                         _ptr(logits) if want_logits else None,
+                                         threads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_lmhead_topk failed (rc={rc})")
+        return (ids, unary, logits) if want_logits else (ids, unary)
 
     def projection(self, hidden_bits: np.ndarray, w_bits: np.ndarray,
                    threads: int | None = None, want_exact: bool = False):
@@ -178,6 +207,11 @@ def edges(pred_bits, succ_bits, cand, unary, h_bits, anchors, threads=None,
           allow_bad_ids=False):
     return get().edges(pred_bits, succ_bits, cand, unary, h_bits, anchors, threads,
                        allow_bad_ids)
+
+
+def lmhead_topk(hidden_bits, lm_head_bits, K, threads=None, softcap=0.0, scale=1.0,
+                want_logits=False):
+    return get().lmhead_topk(hidden_bits, lm_head_bits, K, threads, softcap, scale, want_logits)
 
 
 def selector(logits, hidden_bits, w_bits, pred_bits, succ_bits, anchors, K, threads=None,

@@ -187,6 +187,72 @@ int oracle_topk(const float* logits, int64_t rows, int64_t V, int K, double soft
     return c.failed ? -1 : 0;
 }
 
+/* ---------------------------------------------------------------- candidate head from the LM head */
+
+typedef struct {
+    const uint16_t* hidden;   /* [rows, H] bf16 bits */
+    const uint16_t* lm_head;  /* [V, H] bf16 bits */
+    int64_t H, V;
+    int K;
+    double softcap, scale;
+    int32_t* ids;
+    float* unary;
+    double* logits_out;       /* [rows, V] exact logits, or NULL */
+    int failed;
+} lmhead_ctx;
+
+/* Order of (exact logit, id): the candidate order of the top-k, on fp64 values. */
+typedef struct {
+    double v;
+    int32_t id;
+} dentry_t;
+
+static int dentry_order(const void* pa, const void* pb) {
+    const dentry_t* a = (const dentry_t*)pa;
+    const dentry_t* b = (const dentry_t*)pb;
+    if (a->v != b->v) return a->v > b->v ? -1 : 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id ? 1 : 0);
+}
+
+static void lmhead_row(void* vctx, int64_t r) {
+    lmhead_ctx* c = (lmhead_ctx*)vctx;
+    dentry_t* e = (dentry_t*)malloc((size_t)c->V * sizeof(dentry_t));
+    if (!e) {
+        c->failed = 1;
+        return;
+    }
+    const uint16_t* x = c->hidden + r * c->H;
+    for (int64_t v = 0; v < c->V; ++v) {
+        const uint16_t* w = c->lm_head + v * c->H;   /* LM head row v: [V, H] */
+        double s = 0.0;
+        for (int64_t i = 0; i < c->H; ++i) s += bf16_to_double(w[i]) * bf16_to_double(x[i]);
+        e[v].v = s;
+        e[v].id = (int32_t)v;
+        if (c->logits_out) c->logits_out[r * c->V + v] = s;
+    }
+    qsort(e, (size_t)c->V, sizeof(dentry_t), dentry_order);
+    for (int k = 0; k < c->K; ++k) {
+        c->ids[r * c->K + k] = e[k].id;
+        c->unary[r * c->K + k] = processed_logit((float)e[k].v, c->softcap, c->scale);
+    }
+    free(e);
+}
+
+/* The candidate head of DFlash2BeamForCausalLM.compute_candidates in full:
+ * logits[r, v] = sum_i hidden[r, i] * lm_head[v, i] (exact, fp64), then the K first tokens
+ * of the candidate order (logit descending, id ascending) and their processed logits.
+ * logits_out (may be NULL) receives the exact logits [rows, V]. */
+int oracle_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head, int64_t rows, int64_t H,
+                       int64_t V, int K, double softcap, double scale, int32_t* ids, float* unary,
+                       double* logits_out, int threads) {
+    if (!hidden || !lm_head || !ids || !unary || rows < 0 || H < 1 || V < 1 || K < 1 || K > V)
+        return -1;
+    if (!(scale > 0.0)) return -1;
+    lmhead_ctx c = {hidden, lm_head, H, V, K, softcap, scale, ids, unary, logits_out, 0};
+    parallel_rows(lmhead_row, &c, rows, threads);
+    return c.failed ? -1 : 0;
+}
+
 /* ---------------------------------------------------------------- step 2: projection */
 
 typedef struct {

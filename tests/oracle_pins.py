@@ -401,11 +401,42 @@ def pin_selector_composes(orc, seed: int = 12) -> None:
     assert np.array_equal(h, h2) and np.array_equal(e, e2)
 
 
+def pin_lmhead_topk_vs_numpy(orc, seed: int = 14) -> None:
+    """Against numpy: fp64 matmul of the bf16 values, then a stable sort by (-logit, id)."""
+    g = torch.Generator().manual_seed(seed)
+    rows, H, V, K = 5, 72, 300, 7
+    x = torch.randn(rows, H, generator=g).to(torch.bfloat16)
+    w = (torch.randn(V, H, generator=g) / 8).to(torch.bfloat16)
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    ids, un, logits = orc.lmhead_topk(bits(x), bits(w), K, softcap=4.0, scale=0.5,
+                                      want_logits=True)
+    ref = x.double().numpy() @ w.double().numpy().T
+    assert np.allclose(logits, ref, rtol=0, atol=1e-12)
+    for r in range(rows):
+        want = np.argsort(-ref[r], kind="stable")[:K]
+        assert ids[r].tolist() == want.tolist()
+        v = ref[r][want].astype(np.float32).astype(np.float64)
+        assert np.allclose(un[r], (4.0 * np.tanh(v / 4.0) * 0.5).astype(np.float32), rtol=2e-7)
+
+
+def pin_lmhead_topk_one_hot(orc) -> None:
+    """A one-hot hidden state picks one column of the LM head: logits = lm_head[:, i]."""
+    H, V, K = 16, 40, 5
+    w = np.arange(V * H, dtype=np.float32).reshape(V, H) % 7 - 3.0       # ties on purpose
+    x = np.zeros((1, H), dtype=np.float32)
+    x[0, 3] = 1.0
+    ids, un = orc.lmhead_topk(float_to_bf16_bits_exact(x), float_to_bf16_bits_exact(w), K)
+    col = w[:, 3]
+    want = sorted(range(V), key=lambda v: (-col[v], v))[:K]
+    assert ids[0].tolist() == want and np.array_equal(un[0], col[want])
+
+
 ALL_PINS = [
     pin_topk_golden, pin_topk_bruteforce, pin_topk_stable_sort, pin_topk_invariants,
     pin_topk_logits_processor_golden, pin_topk_logits_processor_vs_numpy,
     pin_bf16_round_cases, pin_bf16_round_vs_torch, pin_bf16_round_nearest,
     pin_projection_golden, pin_projection_closed_forms, pin_projection_vs_numpy,
     pin_edges_golden, pin_edges_zero_codebooks, pin_edges_rank1, pin_edges_structure,
-    pin_edges_vs_einsum, pin_selector_composes,
+    pin_edges_vs_einsum, pin_selector_composes, pin_lmhead_topk_vs_numpy,
+    pin_lmhead_topk_one_hot,
 ]

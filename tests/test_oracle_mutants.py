@@ -19,8 +19,8 @@ from oracle.build import SOURCE, compile_oracle
 # (name, original text, mutated text). Each original must occur exactly once.
 MUTANTS = [
     ("tie_break_reversed",
-     "return (a->id < b->id) ? -1 : (a->id > b->id ? 1 : 0);",
-     "return (a->id > b->id) ? -1 : (a->id < b->id ? 1 : 0);"),
+     "/* -0 == +0 here */\n    return (a->id < b->id) ? -1 : (a->id > b->id ? 1 : 0);",
+     "/* -0 == +0 here */\n    return (a->id > b->id) ? -1 : (a->id < b->id ? 1 : 0);"),
     ("value_order_reversed",
      "return a->v > b->v ? -1 : 1;",
      "return a->v < b->v ? -1 : 1;"),
@@ -43,6 +43,12 @@ MUTANTS = [
     ("processor_not_applied",
      "c->unary[r * c->K + k] = processed_logit(e[k].v, c->softcap, c->scale);",
      "c->unary[r * c->K + k] = e[k].v;"),
+    ("lmhead_transposed",
+     "const uint16_t* w = c->lm_head + v * c->H;   /* LM head row v: [V, H] */",
+     "const uint16_t* w = c->lm_head + v;"),
+    ("lmhead_tie_break_reversed",
+     "return (a->id < b->id) ? -1 : (a->id > b->id ? 1 : 0);\n}\n\nstatic void lmhead_row",
+     "return (a->id > b->id) ? -1 : (a->id < b->id ? 1 : 0);\n}\n\nstatic void lmhead_row"),
     ("projection_weight_transposed",
      "s += bf16_to_double(wj[i]) * bf16_to_double(x[i]);",
      "s += bf16_to_double(c->w[i * c->rank + j]) * bf16_to_double(x[i]); (void)wj;"),
