@@ -22,8 +22,11 @@ MUTANTS = [
      "/* -0 == +0 here */\n    return (a->id < b->id) ? -1 : (a->id > b->id ? 1 : 0);",
      "/* -0 == +0 here */\n    return (a->id > b->id) ? -1 : (a->id < b->id ? 1 : 0);"),
     ("value_order_reversed",
-     "return a->v > b->v ? -1 : 1;",
-     "return a->v < b->v ? -1 : 1;"),
+     "if (ca == 1 && a->v != b->v) return a->v > b->v ? -1 : 1;",
+     "if (ca == 1 && a->v != b->v) return a->v < b->v ? -1 : 1;"),
+    ("lmhead_value_order_reversed",
+     "if (a->v != b->v) return a->v > b->v ? -1 : 1;",
+     "if (a->v != b->v) return a->v < b->v ? -1 : 1;"),
     ("signed_zero_distinct",
      "if (ca == 1 && a->v != b->v) return a->v > b->v ? -1 : 1;",
      "if (ca == 1 && (a->v != b->v || signbit(a->v) != signbit(b->v)))"
