@@ -385,6 +385,71 @@ def run_ours(args, w: wl.Workload) -> None:
         torch.distributed.destroy_process_group()
 
 
+def run_lmhead(args, w: wl.Workload) -> None:
+    """The candidate head straight from the LM head (no logits in memory), one GPU.
+
+    Inputs: the workload's hidden states as the drafter's final hidden state, and a seeded
+    synthetic LM head [V, H] bf16 ~ N(0, 1/sqrt(H)) drawn on the device. For context, the
+    unfused route is timed too: a cuBLAS bf16 GEMM writing the logits, then this library's
+    top-k over them (fp32 logits of the same shape).
+    """
+    import draft_candidate_selector_gb300 as ds
+    dev = torch.device("cuda", dist_env()[2])
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hidden = wl._bf16_normal(0, wl._TAG_HIDDEN, (w.R, w.S, w.H), 1.0).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    lm_head = (torch.randn((w.V, w.H), generator=g, device=dev) / w.H ** 0.5).to(torch.bfloat16)
+    cand = torch.empty((w.R, w.S, w.K), dtype=torch.int32, device=dev)
+    unary = torch.empty((w.R, w.S, w.K), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, ds._native.load().dflash_lmhead_topk_workspace_bytes(w.R, w.S, w.V, w.K)),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        ds.dflash_lmhead_topk(hidden, lm_head, w.K, cand, unary, ws)
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    with ClockSampler(dev) as clocks:
+        ms = timed(step, args.steps)
+    status = ds.dflash_device_status(clear=True)
+    h2 = hidden.reshape(w.rows, w.H)
+    gemm_ms = timed(lambda: torch.matmul(h2, lm_head.t()), max(3, args.steps // 4))
+    logits = torch.empty((w.R, w.S, w.V), dtype=torch.float32, device=dev).normal_()
+    topk_ms = timed(lambda: ds.dflash_topk_candidates(logits, w.K, cand, unary), max(3, args.steps // 4))
+    del logits
+    flops = 2.0 * w.rows * w.V * w.H
+    peak = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peak = float(json.load(f)["bf16_tflops_sustained"])
+    achieved = flops / (ms / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "candidate-head rows/s from the LM head (R*S)", "value": w.rows / (ms / 1e3),
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16 x bf16 -> f32",
+        "data": "synthetic (seeded)", "config": base_config(w, 1),
+        "roofline": {"bound": "tensor", "kernel": "lmhead_topk_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None,
+                     "traffic": None, "peak_source": "measured sustained bf16 (MEASURED_PEAKS.json)"},
+        "unfused_reference": {"cublas_bf16_gemm_ms": gemm_ms, "logits_topk_ms": topk_ms,
+                              "sum_ms": gemm_ms + topk_ms},
+        "gpu_launches": args.steps, "device_status": status, "clocks": clocks.summary(),
+    }), flush=True)
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,6 +459,8 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", default="gemma_large", choices=wl.WORKLOAD_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lmhead", action="store_true",
+                    help="time the candidate head straight from a synthetic LM head instead")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the step captured once in a CUDA graph")
     ap.add_argument("--requests", type=int, default=None,
@@ -407,6 +474,8 @@ def main(argv=None) -> None:
                                 description=f"{w.description}; R overridden to {args.requests}")
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.lmhead:
+        run_lmhead(args, w)
     else:
         run_ours(args, w)
 

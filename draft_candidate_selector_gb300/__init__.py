@@ -24,7 +24,8 @@ from ._native import DEVICE_BAD_ID, DEVICE_TIMEOUT, DflashError  # noqa: F401
 
 __all__ = [
     "dflash_topk_candidates", "dflash_hidden_projection", "dflash_candidate_edges",
-    "dflash_selector", "dflash_topk_workspace_bytes", "dflash_selector_workspace_bytes",
+    "dflash_selector", "dflash_lmhead_topk", "dflash_topk_workspace_bytes",
+    "dflash_selector_workspace_bytes",
     "dflash_device_status", "dflash_trace_begin", "dflash_trace_end", "DflashError",
     "library_path",
 ]
@@ -100,6 +101,33 @@ def dflash_topk_candidates(logits: torch.Tensor, K: int, cand_ids: torch.Tensor 
         _native.check(lib.dflash_topk_candidates(
             _ptr(logits), R, S, V, K, float(softcap), float(scale), _ptr(cand_ids), _ptr(unary),
             _ptr(ws), ws.numel(), _stream(dev, stream)))
+    return cand_ids, unary
+
+
+def dflash_lmhead_topk(hidden: torch.Tensor, lm_head: torch.Tensor, K: int,
+                       cand_ids: torch.Tensor | None = None, unary: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None,
+                       softcap: float = 0.0, scale: float = 1.0):
+    """Top-K candidates of hidden [R, S, H] . lm_head [V, H]^T without materialised logits."""
+    lib = _native.load()
+    if hidden.dim() != 3 or lm_head.dim() != 2:
+        raise ValueError("hidden must be [R, S, H] and lm_head [V, H]")
+    R, S, H = hidden.shape
+    V = lm_head.shape[0]
+    _need(hidden, "hidden", torch.bfloat16)
+    _need(lm_head, "lm_head", torch.bfloat16, (V, H))
+    dev = hidden.device
+    with torch.cuda.device(dev):
+        if cand_ids is None:
+            cand_ids = torch.empty((R, S, K), dtype=torch.int32, device=dev)
+        if unary is None:
+            unary = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+        _need(cand_ids, "cand_ids", torch.int32, (R, S, K))
+        _need(unary, "unary", torch.float32, (R, S, K))
+        ws = _workspace(lib.dflash_lmhead_topk_workspace_bytes(R, S, V, K), dev, workspace)
+        _native.check(lib.dflash_lmhead_topk(
+            _ptr(hidden), _ptr(lm_head), R, S, H, V, K, float(softcap), float(scale),
+            _ptr(cand_ids), _ptr(unary), _ptr(ws), ws.numel(), _stream(dev, stream)))
     return cand_ids, unary
 
 

@@ -35,6 +35,8 @@ SIGNATURES = {
     "dflash_selector_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "dflash_topk_candidates": (_i, [_p, _i, _i, _i, _i, _f, _f, _p, _p, _p, _sz, _p]),
     "dflash_topk_candidates_noalloc": (_i, [_p, _i, _i, _i, _i, _p, _p, _p]),
+    "dflash_lmhead_topk_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "dflash_lmhead_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _f, _f, _p, _p, _p, _sz, _p]),
     "dflash_hidden_projection": (_i, [_p, _p, _i, _i, _i, _i, _p, _p]),
     "dflash_candidate_edges": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
     "dflash_selector": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _f, _p, _p,

@@ -264,6 +264,40 @@ dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, 
     return ok();
 }
 
+size_t dflash_lmhead_topk_workspace_bytes(int R, int S, int V, int K) {
+    if (check_dims_topk(R, S, V, K) != DFLASH_OK) return 0;
+    dflash::DeviceInfo dev;
+    if (current_device(&dev, nullptr) != DFLASH_OK) return 0;
+    return dflash::lmhead_plan(dev, (long long)R * S, V).workspace_bytes();
+}
+
+dflash_status dflash_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head, int R, int S,
+                                 int H, int V, int K, float softcap, float scale,
+                                 int32_t* cand_ids, float* unary, void* workspace,
+                                 size_t workspace_bytes, dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_processor(softcap, scale));
+    if (H < 1) return fail(DFLASH_INVALID_ARGUMENT, "H=%d must be >= 1", H);
+    if (H % 8 != 0) return fail(DFLASH_UNSUPPORTED, "H=%d: must be a multiple of 8", H);
+    DFLASH_TRY(check_ptr(hidden, "hidden"));
+    DFLASH_TRY(check_ptr(lm_head, "lm_head"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr(workspace, "workspace"));
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    const dflash::LmheadPlan plan = dflash::lmhead_plan(dev, (long long)R * S, V);
+    if (workspace_bytes < plan.workspace_bytes())
+        return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
+                    workspace_bytes, plan.workspace_bytes());
+    cudaError_t e = dflash::launch_lmhead_topk(dev, plan, hidden, lm_head, R * S, H, V, K, softcap,
+                                               scale, cand_ids, unary, workspace, status,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "LM-head top-k launch");
+    return ok();
+}
+
 dflash_status dflash_hidden_projection(const uint16_t* hidden, const uint16_t* w_proj, int R,
                                        int S, int H, int rank, uint16_t* h_out,
                                        dflash_stream_t stream) {

@@ -67,4 +67,24 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
                          const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
                          int rank, float* edges, uint32_t* status_word, cudaStream_t stream);
 
+// ---------------------------------------------------------------- LM head + top-k (lmhead.cu)
+
+// How the candidate head from the LM head is cut: one CTA per (128-row tile, vocabulary
+// split); the splits of a row tile are merged by whichever CTA finishes last.
+struct LmheadPlan {
+    int m_tiles = 0;          // ceil(rows / 128)
+    int n_tiles = 0;          // ceil(V / 256)
+    int n_splits = 0;         // vocabulary ranges per row tile
+    size_t counter_bytes = 0; // per-row-tile arrival counters, padded to 256 B
+    size_t partial_bytes = 0; // [m_tiles][n_splits][32][128] uint64 lists (0 if one split)
+    size_t workspace_bytes() const { return counter_bytes + partial_bytes; }
+};
+
+LmheadPlan lmhead_plan(const DeviceInfo& dev, long long rows, int V);
+
+cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, const uint16_t* hidden,
+                               const uint16_t* lm_head, int M, int H, int V, int K, float softcap,
+                               float scale, int32_t* cand_ids, float* unary, void* workspace,
+                               uint32_t* status_word, cudaStream_t stream);
+
 }  // namespace dflash

@@ -1,0 +1,369 @@
+// lmhead.cu: the candidate head straight from the LM head. The top-K of
+// logits = hidden . lm_head^T is taken without writing the logits anywhere.
+//
+// Method: page "vllm.models.beam.nvidia.dflash2", DFlash2BeamForCausalLM.compute_candidates:
+// get_top_k_tokens(lm_head, hidden, top_k) yields the selector's top-k candidate ids and their
+// logits at each position. The candidate order and the logits processor's options are those
+// of the logits top-k (topk.cu). The logits are fp32 sums of bf16 products, taken by the
+// tensor cores.
+//
+// GEMM view: logits[M = R*S, N = V] = hidden[M, H] . lm_head[V, H]^T, both operands
+// K-major. One CTA (6 warps, one per SM) owns a 128-row tile of M and a contiguous range of
+// 256-wide vocabulary tiles:
+//   * warp 0, one lane: TMA producer. It streams 128x64 hidden tiles and 256x64 LM-head
+//     tiles (128-byte swizzle) through a 4-stage shared-memory ring. All CTAs that share a
+//     vocabulary range walk it in step, so each LM-head tile comes from HBM once and is
+//     reused from L2.
+//   * warp 1, one lane: MMA issuer. tcgen05.mma kind::f16 (bf16 x bf16 -> fp32),
+//     M = 128, N = 256, K = 16, into one of two 256-column accumulators in tensor memory.
+//     The epilogue drains one while the next tile accumulates in the other.
+//   * warps 2-5: epilogue, one thread per row (tensor-memory lane). Each reads its row's
+//     256 logits of the tile (tcgen05.ld, 32 columns at a time). A float compare against its
+//     K-th best so far rejects almost all of them. Survivors enter the row's sorted list,
+//     kept in shared memory (k-major, so lanes hit distinct banks).
+// When a CTA has finished its range, it writes its lists to the workspace. The CTA of a row
+// tile that arrives last merges all of them and writes the K candidates. Nobody waits on
+// another CTA. Every mbarrier wait is bounded (about a second); on expiry the CTA sets
+// kStatusTimeout and stops.
+#include "common.cuh"
+#include "ptx.cuh"
+
+#include <algorithm>
+#include <mutex>
+
+namespace dflash {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;                       // bf16 elements per 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreads = 192;                // producer, MMA, 4 epilogue warps
+constexpr int kMaxK = 32;
+constexpr uint32_t kATile = BM * BK * 2;     // 16 KB
+constexpr uint32_t kBTile = BN * BK * 2;     // 32 KB
+constexpr uint32_t kTmemCols = 2 * BN;       // two accumulators
+
+__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
+    bits = (bits == 0x80000000u) ? 0u : bits;
+    uint32_t k = bits ^ ((uint32_t)((int32_t)bits >> 31) | 0x80000000u);
+    return min(max(k, 0x007FFFFEu), 0xFF800001u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+    uint32_t bits = (key & 0x80000000u) ? (key ^ 0x80000000u) : ~key;
+    return __uint_as_float(bits);
+}
+
+__device__ __forceinline__ float processed(float x, float softcap, float scale) {
+    if (softcap > 0.f) x = softcap * tanhf(x / softcap);
+    return x * scale;
+}
+
+struct LmSmem {
+    uint32_t a, b, lists, bars, slot, flag, total;
+};
+
+__host__ __device__ inline LmSmem lm_smem_layout() {
+    LmSmem L;
+    L.a = 0;                                             // kStages x 16 KB
+    L.b = L.a + kStages * kATile;                        // kStages x 32 KB
+    L.lists = L.b + kStages * kBTile;                    // [kMaxK][128] uint64
+    L.bars = L.lists + kMaxK * BM * 8;                   // full, empty, tfull[2], tempty[2]
+    L.slot = L.bars + (2 * kStages + 4) * 8;             // tensor-memory base address
+    L.flag = L.slot + 8;                                 // "this CTA merges" flag
+    L.total = L.flag + 8;
+    return L;
+}
+
+// Insert entry c into the descending list of this thread's row (length K, k-major in smem).
+__device__ __forceinline__ void list_insert(uint64_t* lst, int t, int K, uint64_t c) {
+    int pos = K - 1;
+    while (pos > 0) {
+        const uint64_t prev = lst[(pos - 1) * BM + t];
+        if (prev >= c) break;
+        lst[pos * BM + t] = prev;
+        --pos;
+    }
+    lst[pos * BM + t] = c;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   int M, int H, int V, int K, int n_tiles, int n_splits, float softcap,
+                   float scale, int32_t* __restrict__ cand_ids, float* __restrict__ unary,
+                   uint32_t* __restrict__ counters, uint64_t* __restrict__ partials,
+                   uint32_t* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const LmSmem L = lm_smem_layout();
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* tfull = bars + 2 * kStages;
+    uint64_t* tempty = bars + 2 * kStages + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.slot);
+    int* merge_flag = reinterpret_cast<int*>(smem + L.flag);
+    uint64_t* lst = reinterpret_cast<uint64_t*>(smem + L.lists);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x / n_splits;
+    const int split = blockIdx.x % n_splits;
+    const int n_begin = (int)((long long)split * n_tiles / n_splits);
+    const int n_end = (int)((long long)(split + 1) * n_tiles / n_splits);
+    const int T = n_end - n_begin;                       // vocabulary tiles of this CTA
+    const int num_kb = (H + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), BM);        // every epilogue thread arrives
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
+        *merge_flag = 0;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            long long g = 0;
+            bool ok = true;
+            for (int t = 0; t < T && ok; ++t) {
+                const int n0 = (n_begin + t) * BN;
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    const int s = (int)(g % kStages);
+                    if (g >= kStages &&
+                        !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((g / kStages) - 1) & 1))) {
+                        atomicOr(status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_expect_tx(fb, kATile + kBTile);
+                    tma_load_2d(smem_u32(smem + L.a + s * kATile), &map_a, fb, kb * BK, m_tile * BM);
+                    tma_load_2d(smem_u32(smem + L.b + s * kBTile), &map_b, fb, kb * BK, n0);
+                }
+            }
+            // Let the last loads land before this thread leaves the role.
+            const long long issued = g;
+            for (long long q = std::max(0LL, issued - kStages); q < issued; ++q)
+                (void)mbar_wait(smem_u32(&full[q % kStages]), (uint32_t)((q / kStages) & 1));
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer
+            const uint32_t idesc = f16_idesc(BM, BN);
+            long long g = 0;
+            bool ok = true;
+            for (int t = 0; t < T && ok; ++t) {
+                const int buf = t & 1;
+                if (t >= 2 &&
+                    !mbar_wait(smem_u32(&tempty[buf]), (uint32_t)(((t >> 1) - 1) & 1))) {
+                    atomicOr(status, kStatusTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(buf * BN);
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    const int s = (int)(g % kStages);
+                    if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((g / kStages) & 1))) {
+                        atomicOr(status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + L.a + s * kATile);
+                    const uint32_t b0 = smem_u32(smem + L.b + s * kBTile);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16(acc, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
+                                  (kb | k) != 0);
+                    umma_commit(smem_u32(&empty[s]));
+                }
+                umma_commit(smem_u32(&tfull[buf]));
+            }
+        }
+    } else {
+        // ---- epilogue: thread = row (tensor-memory lane) of the tile
+        const int quad = warp & 3;                       // lanes 32*quad .. 32*quad + 31
+        const int t_row = quad * 32 + lane;              // 0..127
+        for (int k = 0; k < K; ++k) lst[k * BM + t_row] = 0;   // sentinel: below every entry
+        uint64_t thr = 0;
+        float thr_f = __uint_as_float(0xFFFFFFFFu);      // NaN: everything passes at first
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int buf = t & 1;
+            const bool ready = __all_sync(0xffffffffu,
+                                          mbar_wait(smem_u32(&tfull[buf]), (uint32_t)((t >> 1) & 1)));
+            if (!ready) {
+                if (lane == 0) atomicOr(status, kStatusTimeout);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t n0 = (uint32_t)(n_begin + t) * BN;
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c0), v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float x = __uint_as_float(v[j]);
+                    if (!(x < thr_f)) {                  // conservative: NaN and ties pass
+                        const uint32_t id = n0 + (uint32_t)(c0 + j);
+                        const uint64_t e = ((uint64_t)order_key(v[j]) << 32) | (uint32_t)(~id);
+                        if (id < (uint32_t)V && e > thr) {
+                            list_insert(lst, t_row, K, e);
+                            thr = lst[(K - 1) * BM + t_row];
+                            thr_f = key_value((uint32_t)(thr >> 32));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty[buf]));
+        }
+
+        // ---- this CTA's lists -> final candidates, or partials merged by the last CTA
+        const long long row = (long long)m_tile * BM + t_row;
+        bool write_final = ok && n_splits == 1;
+        if (n_splits > 1) {
+            // The named barriers run in every epilogue thread, even after a timeout, so no
+            // thread can be left waiting at one. A CTA that timed out still arrives; its
+            // lists are then wrong, and the status word says so.
+            uint64_t* mine = partials + ((long long)m_tile * n_splits + split) * kMaxK * BM;
+            for (int k = 0; k < K; ++k) mine[k * BM + t_row] = lst[k * BM + t_row];
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+            if (t_row == 0) {
+                const unsigned arrived = atomicAdd(&counters[m_tile], 1u);
+                *merge_flag = (arrived == (unsigned)(n_splits - 1)) ? 1 : 0;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (*merge_flag) {
+                __threadfence();
+                for (int sp = 0; sp < n_splits; ++sp) {
+                    if (sp == split) continue;
+                    const unsigned long long* other = reinterpret_cast<const unsigned long long*>(
+                        partials + ((long long)m_tile * n_splits + sp) * kMaxK * BM);
+                    for (int k = 0; k < K; ++k) {
+                        const uint64_t e = __ldcg(other + k * BM + t_row);
+                        if (e > lst[(K - 1) * BM + t_row]) list_insert(lst, t_row, K, e);
+                    }
+                }
+                write_final = true;
+            }
+        }
+        if (write_final && row < M) {
+            for (int k = 0; k < K; ++k) {
+                const uint64_t e = lst[k * BM + t_row];
+                cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
+                unary[row * K + k] = processed(key_value((uint32_t)(e >> 32)), softcap, scale);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128-byte swizzle.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+               uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+LmheadPlan lmhead_plan(const DeviceInfo& dev, long long rows, int V) {
+    LmheadPlan p;
+    p.m_tiles = (int)((rows + BM - 1) / BM);
+    p.n_tiles = (V + BN - 1) / BN;
+    p.n_splits = std::max(1, std::min(p.n_tiles, std::max(1, dev.sm_count) / std::max(1, p.m_tiles)));
+    p.counter_bytes = (size_t)((p.m_tiles * 4 + 255) / 256 * 256);
+    p.partial_bytes = p.n_splits > 1 ? (size_t)p.m_tiles * p.n_splits * kMaxK * BM * 8 : 0;
+    return p;
+}
+
+cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, const uint16_t* hidden,
+                               const uint16_t* lm_head, int M, int H, int V, int K, float softcap,
+                               float scale, int32_t* cand_ids, float* unary, void* workspace,
+                               uint32_t* status_word, cudaStream_t stream) {
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    const size_t smem = 1024 + lm_smem_layout().total;
+    std::call_once(once[dev.device], [&] {
+        attr_err[dev.device] = cudaFuncSetAttribute(
+            lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
+    CUtensorMap map_a, map_b;
+    if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
+        !encode_2d(&map_b, lm_head, (uint64_t)V, (uint64_t)H, BN))
+        return cudaErrorInvalidValue;
+    uint32_t* counters = static_cast<uint32_t*>(workspace);
+    uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + plan.counter_bytes);
+    cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
+    if (err != cudaSuccess) return err;
+    lmhead_topk_kernel<<<plan.m_tiles * plan.n_splits, kThreads, smem, stream>>>(
+        map_a, map_b, M, H, V, K, plan.n_tiles, plan.n_splits, softcap, scale, cand_ids, unary,
+        counters, partials, status_word);
+    return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -118,6 +118,31 @@ dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, 
                                              dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * Step 1 from the LM head: the candidate head without materialised logits.
+ * Source: DFlash2BeamForCausalLM.compute_candidates, which calls
+ * LogitsProcessor.get_top_k_tokens(lm_head, hidden_states, top_k).
+ *
+ * hidden    [R, S, H] bf16   drafter hidden states
+ * lm_head   [V, H]    bf16   the LM head weight (vocabulary rows)
+ * cand_ids  [R, S, K] int32  out: the K best token ids of each row, in candidate order
+ * unary     [R, S, K] float  out: their (processed) logits
+ * workspace                  at least dflash_lmhead_topk_workspace_bytes(R, S, V, K) bytes;
+ *                            its contents on entry do not matter.
+ *
+ * logits[r,p,v] = sum_i hidden[r,p,i] * lm_head[v,i] are fp32 sums taken by the tensor
+ * cores (tcgen05, operands staged by TMA). They never leave the chip. The candidate order,
+ * softcap and scale are those of dflash_topk_candidates. Where two logits differ by less
+ * than their fp32 accumulation error, their order may differ from an exact computation.
+ * Requires H a multiple of 8.
+ * ---------------------------------------------------------------------------------- */
+size_t dflash_lmhead_topk_workspace_bytes(int R, int S, int V, int K);
+
+dflash_status dflash_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head, int R, int S,
+                                 int H, int V, int K, float softcap, float scale,
+                                 int32_t* cand_ids, float* unary, void* workspace,
+                                 size_t workspace_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Step 2: hidden projection, h = hidden . W_proj^T with no bias.
  * Source: DFlash2BeamCandidateSelector.__init__ (hidden_projection: a bias-free linear
  * map hidden_size -> rank, in params_dtype) and forward (hidden must be bf16).

@@ -123,3 +123,55 @@ def sample_requests(R: int, k: int, seed: int) -> np.ndarray:
     pick = set(int(x) for x in rng.choice(R, size=min(k, R), replace=False))
     pick.update([0, R - 1])
     return np.array(sorted(pick), dtype=np.int64)
+
+
+def assert_lmhead_valid(gpu_ids: np.ndarray, gpu_unary: np.ndarray, hidden_bits: np.ndarray,
+                        lm_head_bits: np.ndarray, K: int, what: str, softcap: float = 0.0,
+                        scale: float = 1.0) -> float:
+    """Candidates from fp32 tensor-core logits, checked against the exact logits.
+
+    tol_v = 2 * H * 2^-24 * sum_i |x_i w_vi| bounds how far two fp32 sums can reorder.
+    (a) every chosen id is in range and distinct, and its exact logit is within tol of the
+        exact K-th best;
+    (b) every id that beats the exact (K+1)-th best by more than tol is chosen;
+    (c) the chosen order never puts a logit below the next one by more than tol;
+    (d) the unary values are within 2e-3 * (1 + |ref|) of the processed exact logits.
+    Returns the fraction of rows whose ids equal the oracle's exactly.
+    """
+    H = hidden_bits.shape[-1]
+    V = lm_head_bits.shape[0]
+    x = bits_to_f64(hidden_bits).reshape(-1, H)
+    w = bits_to_f64(lm_head_bits).reshape(V, H)
+    ref_ids, _, exact = oracle.lmhead_topk(hidden_bits.reshape(-1, H), lm_head_bits, K,
+                                           softcap=softcap, scale=scale, want_logits=True)
+    tol = 2.0 * H * 2.0 ** -24 * (np.abs(x) @ np.abs(w).T)
+    gi = np.asarray(gpu_ids).reshape(-1, K)
+    gu = np.asarray(gpu_unary, dtype=np.float64).reshape(-1, K)
+    same = 0
+    for r in range(gi.shape[0]):
+        ids = gi[r]
+        assert np.all((ids >= 0) & (ids < V)), f"{what}: row {r} has an id out of range"
+        assert len(set(ids.tolist())) == K, f"{what}: row {r} repeats an id"
+        L = exact[r]
+        order = ref_ids[r]
+        kth = L[order[K - 1]]
+        nxt = np.sort(L)[::-1][K] if V > K else -np.inf
+        t = tol[r]
+        assert np.all(L[ids] + t[ids] + t[order[K - 1]] >= kth), f"{what}: row {r} chose a loser"
+        must = np.nonzero(L > nxt + t + t.max())[0]
+        assert set(must.tolist()) <= set(ids.tolist()), f"{what}: row {r} missed a clear winner"
+        assert np.all(L[ids[:-1]] + t[ids[:-1]] + t[ids[1:]] >= L[ids[1:]]), \
+            f"{what}: row {r} out of order"
+        v = L[ids].astype(np.float32).astype(np.float64)
+        ref_u = (softcap * np.tanh(v / softcap) if softcap > 0 else v) * scale
+        assert np.all(np.abs(gu[r] - ref_u) <= RTOL * (1 + np.abs(ref_u)) + 2 * t[ids] * scale), \
+            f"{what}: row {r} unary off"
+        same += int(np.array_equal(ids, order))
+    return same / gi.shape[0]
+
+
+def float_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bits of float32 values that are exactly representable in bf16 (checked)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0)
+    return (u >> 16).astype(np.uint16)

@@ -410,3 +410,54 @@ def test_selector_logits_processor(dev, name):
     P.assert_projection(P.bits(h), P.bits(inp.hidden), P.bits(inp.w_proj), f"{name} h")
     P.assert_close(e.cpu().numpy(), r_e, f"{name} edges")
     _status_clean()
+
+
+# ----------------------------------------------------------------------------- candidate head from the LM head
+
+def _bf16(t):
+    return t.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,H,V,K", [
+    (7, 64, 300, 4),          # one row tile, two vocabulary tiles
+    (130, 520, 8000, 8),      # ragged rows, K and V; 32 vocabulary splits of one tile each
+    (300, 256, 3000, 32),     # K = 32
+    (2560, 64, 20000, 16),    # 20 row tiles, 7 splits: about 11 tiles per CTA
+])
+def test_lmhead_topk_valid(dev, rows, H, V, K):
+    g = torch.Generator().manual_seed(rows + V)
+    hid = _bf16(torch.randn(1, rows, H, generator=g))
+    w = _bf16(torch.randn(V, H, generator=g) / H ** 0.5)
+    ids, un = ds.dflash_lmhead_topk(hid.to(dev), w.to(dev), K)
+    same = P.assert_lmhead_valid(ids.cpu().numpy(), un.cpu().numpy(), P.bits(hid), P.bits(w), K,
+                                 f"rows={rows} H={H} V={V} K={K}")
+    assert same > 0.9, f"only {same:.2f} of rows match the exact order"
+    _status_clean()
+
+
+def test_lmhead_topk_one_hot_exact(dev):
+    """One-hot hidden states make every logit an exact LM-head entry: no rounding at all, so
+    the ids must equal the oracle's, ties (planted in the LM head) included."""
+    rows, H, V, K = 200, 128, 5000, 16
+    rng = np.random.default_rng(5)
+    hot = rng.integers(0, H, rows)
+    x = np.zeros((1, rows, H), dtype=np.float32)
+    x[0, np.arange(rows), hot] = rng.choice([1.0, -1.0, 0.5, 2.0], rows)
+    w = rng.integers(-6, 7, size=(V, H)).astype(np.float32) / 4   # many exact ties
+    xb, wb = P.float_bits(x), P.float_bits(w)
+    ids, un = ds.dflash_lmhead_topk(torch.from_numpy(x).to(torch.bfloat16).to(dev),
+                                    torch.from_numpy(w).to(torch.bfloat16).to(dev), K)
+    ref_ids, ref_un = oracle.lmhead_topk(xb.reshape(rows, H), wb, K)
+    P.assert_ids_equal(ids.cpu().numpy().reshape(rows, K), ref_ids, "one-hot ids")
+    P.assert_close(un.cpu().numpy().reshape(rows, K), ref_un, "one-hot unary")
+    _status_clean()
+
+
+def test_lmhead_topk_logits_processor(dev):
+    g = torch.Generator().manual_seed(3)
+    rows, H, V, K = 64, 96, 2000, 8
+    hid = _bf16(torch.randn(1, rows, H, generator=g) * 4)
+    w = _bf16(torch.randn(V, H, generator=g))
+    ids, un = ds.dflash_lmhead_topk(hid.to(dev), w.to(dev), K, softcap=5.0, scale=0.5)
+    P.assert_lmhead_valid(ids.cpu().numpy(), un.cpu().numpy(), P.bits(hid), P.bits(w), K,
+                          "lm head with soft cap", softcap=5.0, scale=0.5)
