@@ -323,14 +323,37 @@ def run_ours(args, w: wl.Workload) -> None:
     h2d = logits_host.nbytes + hidden_host.nbytes + anchors_host.nbytes
     d2h = out_edges.nbytes + out_cand.nbytes + out_unary.nbytes
 
+    # End to end, pipelined by chunks of requests (they are independent): the inputs of
+    # chunk c+1 copy in on one stream while the selector runs on chunk c, and outputs copy
+    # out on a third stream. The host link, not the kernels, bounds this number.
+    nch = max(1, min(args.e2e_chunks, w.R))
+    bounds = [w.R * c // nch // 4 * 4 for c in range(nch)] + [w.R]   # 16-byte aligned chunks
+    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(nch)]
+    ev_done = [torch.cuda.Event() for _ in range(nch)]
+
     def e2e_step():
-        logits.copy_(logits_host, non_blocking=True)
-        hidden.copy_(hidden_host, non_blocking=True)
-        anchors.copy_(anchors_host, non_blocking=True)
-        step()
-        out_edges.copy_(edges, non_blocking=True)
-        out_cand.copy_(cand, non_blocking=True)
-        out_unary.copy_(unary, non_blocking=True)
+        for c in range(nch):
+            r0, r1 = bounds[c], bounds[c + 1]
+            if r1 <= r0:
+                continue
+            with torch.cuda.stream(copy_in):
+                logits[r0:r1].copy_(logits_host[r0:r1], non_blocking=True)
+                hidden[r0:r1].copy_(hidden_host[r0:r1], non_blocking=True)
+                anchors[r0:r1].copy_(anchors_host[r0:r1], non_blocking=True)
+                ev_in[c].record(copy_in)
+            stream.wait_event(ev_in[c])
+            ds.dflash_selector(logits[r0:r1], hidden[r0:r1], w_proj, pred_cb, succ_cb,
+                               anchors[r0:r1], w.K, cand[r0:r1], unary[r0:r1], h[r0:r1],
+                               edges[r0:r1], ws)
+            ev_done[c].record(stream)
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(ev_done[c])
+                out_edges[r0:r1].copy_(edges[r0:r1], non_blocking=True)
+                out_cand[r0:r1].copy_(cand[r0:r1], non_blocking=True)
+                out_unary[r0:r1].copy_(unary[r0:r1], non_blocking=True)
+        stream.wait_stream(copy_out)
+        copy_in.wait_stream(stream)     # the next step's copies wait for this step's kernels
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -373,7 +396,9 @@ def run_ours(args, w: wl.Workload) -> None:
                           "source": stages_source},
             "launch_mode": "cuda_graph_replay" if graph is not None else "eager",
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "pipeline_chunks": nch,
+                    "h2d_gbs_effective": h2d / (e2e_ms / 1e3) / 1e9},
             "gpu_launches": 3 * args.steps,   # projection, top-k, edges per step
             "device_status": status,
             "clocks": clocks.summary(),
@@ -458,6 +483,8 @@ def main(argv=None) -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemma_large", choices=wl.WORKLOAD_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="request chunks the end-to-end loop pipelines copies and kernels over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lmhead", action="store_true",
                     help="time the candidate head straight from a synthetic LM head instead")
