@@ -461,3 +461,53 @@ def test_lmhead_topk_logits_processor(dev):
     ids, un = ds.dflash_lmhead_topk(hid.to(dev), w.to(dev), K, softcap=5.0, scale=0.5)
     P.assert_lmhead_valid(ids.cpu().numpy(), un.cpu().numpy(), P.bits(hid), P.bits(w), K,
                           "lm head with soft cap", softcap=5.0, scale=0.5)
+
+
+# ----------------------------------------------------------------------------- robustness
+
+def test_topk_fuzz_shapes(dev):
+    """Seeded random shapes (rows, V, K) against the oracle: spans, row splits and ragged
+    heads and tails land in many different places."""
+    rng = np.random.default_rng(2024)
+    for trial in range(24):
+        V = int(rng.choice([int(rng.integers(1, 200)), int(rng.integers(200, 70000))]))
+        K = int(rng.integers(1, min(32, V) + 1))
+        R, S = int(rng.integers(1, 6)), int(rng.integers(1, 9))
+        scale = float(rng.choice([0.5, 3.0, 40.0]))
+        x = (rng.standard_normal((R, S, V)) * scale).astype(np.float32)
+        if trial % 3 == 0:
+            x = np.round(x)                               # ties
+        _topk_case(dev, x, K, f"fuzz {trial}: R={R} S={S} V={V} K={K}")
+
+
+def test_selector_concurrent_streams(dev):
+    """Two host threads call the fused selector at once on two streams. The shared side
+    stream of the projection must not mix their work: each result equals a lone call's."""
+    import threading
+    inp = [wl.make_inputs(RAGGED, seed=s) for s in (0, 1)]
+    w = RAGGED
+    d = [P.to_device(i, dev) for i in inp]
+    ref = [ds.dflash_selector(x["logits"], x["hidden"], x["w_proj"], x["pred_cb"], x["succ_cb"],
+                              x["anchors"], w.K) for x in d]
+    torch.cuda.synchronize(dev)
+    out = [None, None]
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+
+    def run(i):
+        torch.cuda.set_device(dev)
+        with torch.cuda.stream(streams[i]):
+            for _ in range(20):
+                out[i] = ds.dflash_selector(d[i]["logits"], d[i]["hidden"], d[i]["w_proj"],
+                                            d[i]["pred_cb"], d[i]["succ_cb"], d[i]["anchors"],
+                                            w.K, stream=streams[i])
+        streams[i].synchronize()
+
+    th = [threading.Thread(target=run, args=(i,)) for i in (0, 1)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    for i in (0, 1):
+        for a, b in zip(out[i], ref[i]):
+            assert torch.equal(a, b), f"thread {i}: a result differs from the lone call"
+    _status_clean()
