@@ -33,6 +33,7 @@ struct TopkPlan {
     int warps = 0;            // warps with work
     int blocks = 0;           // CTAs launched
     long long rows = 0;       // R * S
+    int variant = 0;          // kernel build: 0 targets 3 CTAs per SM, 1 targets 2
     size_t counter_bytes = 0; // per-row arrival counters (uint32), padded to 256 B
     size_t partial_bytes = 0; // two 32-entry partial lists (uint64) per warp
     size_t workspace_bytes() const { return counter_bytes + partial_bytes; }
