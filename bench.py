@@ -381,7 +381,9 @@ def run_ours(args, w: wl.Workload) -> None:
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32 logits / bf16 x bf16 -> f32 projection and edges",
+            "dtype": "f32",
+            "dtype_detail": "f32 logits compared in f32; projection and edges: bf16 inputs, "
+                            "f32 products and sums",
             "data": "synthetic (seeded, shapes and distributions of the workload)",
             "config": base_config(w, world),
             "roofline": {"bound": "hbm", "kernel": "topk_kernel", "achieved": achieved,
