@@ -109,3 +109,26 @@ def test_python_errors_map_to_exceptions(lib):
         _native.check(_native.DFLASH_UNSUPPORTED)
     with pytest.raises(_native.DflashError):
         _native.check(_native.DFLASH_CUDA_ERROR)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the compiled library the binding raises instead of computing."""
+    monkeypatch.setattr(_native, "_lib", None)
+    monkeypatch.setattr(_native._build, "LIBRARY", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _native.load(build_if_needed=False)
+
+
+def test_trace_end_without_begin(lib):
+    n = ctypes.c_int(7)
+    assert lib.dflash_trace_end(None, 0, ctypes.byref(n)) == _native.DFLASH_INVALID_ARGUMENT
+    assert lib.dflash_trace_begin(0) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_lmhead_argument_checks(lib):
+    f = lib.dflash_lmhead_topk
+    assert f(A, A, 2, 3, 60, 1000, 8, 0.0, 1.0, A, A, A, 1 << 20, None) == _native.DFLASH_UNSUPPORTED
+    assert f(A, A, 2, 3, 64, 1000, 40, 0.0, 1.0, A, A, A, 1 << 20, None) == _native.DFLASH_UNSUPPORTED
+    assert f(A, A, 2, 3, 64, 4, 8, 0.0, 1.0, A, A, A, 1 << 20, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(A, MIS, 2, 3, 64, 1000, 8, 0.0, 1.0, A, A, A, 1 << 20, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(A, A, 2, 3, 64, 1000, 8, 0.0, -1.0, A, A, A, 1 << 20, None) == _native.DFLASH_INVALID_ARGUMENT
