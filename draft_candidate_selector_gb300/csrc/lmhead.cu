@@ -18,9 +18,12 @@
 //     M = 128, N = 256, K = 16, into one of two 256-column accumulators in tensor memory.
 //     The epilogue drains one while the next tile accumulates in the other.
 //   * warps 2-5: epilogue, one thread per row (tensor-memory lane). Each reads its row's
-//     256 logits of the tile (tcgen05.ld, 32 columns at a time). A float compare against its
-//     K-th best so far rejects almost all of them. Survivors enter the row's sorted list,
-//     kept in shared memory (k-major, so lanes hit distinct banks).
+//     256 logits of the tile (tcgen05.ld, 32 columns at a time). One float compare per value
+//     against the row's KC-th best so far turns the 32 values into a bit mask of survivors,
+//     which is empty almost always. The thread then walks only its own survivors, so a warp
+//     spends as many steps as its busiest row has survivors. Each survivor goes into the
+//     row's sorted list, held in registers (KC = 8, 16 or 32 entries, the smallest that holds
+//     K) and updated by a branch-free network of min/max steps.
 // When a CTA has finished its range, it writes its lists to the workspace. The CTA of a row
 // tile that arrives last merges all of them and writes the K candidates. Nobody waits on
 // another CTA. Every mbarrier wait is bounded (about a second); on expiry the CTA sets
@@ -63,33 +66,50 @@ __device__ __forceinline__ float processed(float x, float softcap, float scale) 
 }
 
 struct LmSmem {
-    uint32_t a, b, lists, bars, slot, flag, total;
+    uint32_t a, b, bars, slot, flag, total;
 };
 
 __host__ __device__ inline LmSmem lm_smem_layout() {
     LmSmem L;
     L.a = 0;                                             // kStages x 16 KB
     L.b = L.a + kStages * kATile;                        // kStages x 32 KB
-    L.lists = L.b + kStages * kBTile;                    // [kMaxK][128] uint64
-    L.bars = L.lists + kMaxK * BM * 8;                   // full, empty, tfull[2], tempty[2]
+    L.bars = L.b + kStages * kBTile;                     // full, empty, tfull[2], tempty[2]
     L.slot = L.bars + (2 * kStages + 4) * 8;             // tensor-memory base address
     L.flag = L.slot + 8;                                 // "this CTA merges" flag
     L.total = L.flag + 8;
     return L;
 }
 
-// Insert entry c into the descending list of this thread's row (length K, k-major in smem).
-__device__ __forceinline__ void list_insert(uint64_t* lst, int t, int K, uint64_t c) {
-    int pos = K - 1;
-    while (pos > 0) {
-        const uint64_t prev = lst[(pos - 1) * BM + t];
-        if (prev >= c) break;
-        lst[pos * BM + t] = prev;
-        --pos;
-    }
-    lst[pos * BM + t] = c;
+__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t min64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// Insert c into the descending register list l, keeping its KC largest entries. Slot i takes
+// max(l[i], min(l[i-1], c)), all from the old values: the slots above c keep their entries,
+// c lands in its place and the rest move down by one. Fully unrolled, so l stays in
+// registers; no branches.
+template <int KC>
+__device__ __forceinline__ void reg_insert(uint64_t (&l)[KC], uint64_t c) {
+#pragma unroll
+    for (int i = KC - 1; i > 0; --i) l[i] = max64(l[i], min64(l[i - 1], c));
+    l[0] = max64(l[0], c);
 }
 
+// v[j] for a run-time j: a tree of selects on the bits of j (indexing a register array with
+// a run-time index would move it to local memory).
+__device__ __forceinline__ uint32_t pick32(const uint32_t (&v)[32], int j) {
+    uint32_t a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = (j & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (j & 2) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = (j & 4) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) a[i] = (j & 8) ? a[2 * i + 1] : a[2 * i];
+    return (j & 16) ? a[1] : a[0];
+}
+
+template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    int M, int H, int V, int K, int n_tiles, int n_splits, float softcap,
@@ -107,7 +127,6 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     uint64_t* tempty = bars + 2 * kStages + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.slot);
     int* merge_flag = reinterpret_cast<int*>(smem + L.flag);
-    uint64_t* lst = reinterpret_cast<uint64_t*>(smem + L.lists);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -208,8 +227,9 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         // ---- epilogue: thread = row (tensor-memory lane) of the tile
         const int quad = warp & 3;                       // lanes 32*quad .. 32*quad + 31
         const int t_row = quad * 32 + lane;              // 0..127
-        for (int k = 0; k < K; ++k) lst[k * BM + t_row] = 0;   // sentinel: below every entry
-        uint64_t thr = 0;
+        uint64_t lst[KC];                                // descending; 0 is below every entry
+#pragma unroll
+        for (int k = 0; k < KC; ++k) lst[k] = 0;
         float thr_f = __uint_as_float(0xFFFFFFFFu);      // NaN: everything passes at first
         bool ok = true;
         for (int t = 0; t < T; ++t) {
@@ -225,26 +245,34 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             const uint32_t n0 = (uint32_t)(n_begin + t) * BN;
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
+                __syncwarp();
                 tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c0), v);
+                // A value equal to the threshold cannot enter: ids arrive in ascending order,
+                // so it ties with the KC-th entry and loses on the id. NaN passes (exact
+                // order in the key), and so does everything while the list has free slots.
+                uint32_t pass = 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float x = __uint_as_float(v[j]);
-                    if (!(x < thr_f)) {                  // conservative: NaN and ties pass
-                        const uint32_t id = n0 + (uint32_t)(c0 + j);
-                        const uint64_t e = ((uint64_t)order_key(v[j]) << 32) | (uint32_t)(~id);
-                        if (id < (uint32_t)V && e > thr) {
-                            list_insert(lst, t_row, K, e);
-                            thr = lst[(K - 1) * BM + t_row];
-                            thr_f = key_value((uint32_t)(thr >> 32));
-                        }
-                    }
+                for (int j = 0; j < 32; ++j)
+                    pass |= (__uint_as_float(v[j]) <= thr_f ? 0u : 1u) << j;
+                const uint32_t id0 = n0 + (uint32_t)c0;
+                if (id0 + 32u > (uint32_t)V)                 // the zero-filled tail past V
+                    pass &= (id0 >= (uint32_t)V) ? 0u : ((1u << ((uint32_t)V - id0)) - 1u);
+                while (pass) {
+                    const int j = __ffs(pass) - 1;
+                    pass &= pass - 1;
+                    const uint64_t e = ((uint64_t)order_key(pick32(v, j)) << 32) |
+                                       (uint32_t)(~(id0 + (uint32_t)j));
+                    if (e > lst[KC - 1]) reg_insert(lst, e);
                 }
+                thr_f = key_value((uint32_t)(lst[KC - 1] >> 32));
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[buf]));
         }
 
-        // ---- this CTA's lists -> final candidates, or partials merged by the last CTA
+        // ---- this CTA's lists -> final candidates, or partials merged by the last CTA.
+        // Every CTA's own top K holds all of the row's top K that fall in its range, so the
+        // merge of the partial top-K lists is exact.
         const long long row = (long long)m_tile * BM + t_row;
         bool write_final = ok && n_splits == 1;
         if (n_splits > 1) {
@@ -252,7 +280,9 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             // thread can be left waiting at one. A CTA that timed out still arrives; its
             // lists are then wrong, and the status word says so.
             uint64_t* mine = partials + ((long long)m_tile * n_splits + split) * kMaxK * BM;
-            for (int k = 0; k < K; ++k) mine[k * BM + t_row] = lst[k * BM + t_row];
+#pragma unroll
+            for (int k = 0; k < KC; ++k)
+                if (k < K) mine[k * BM + t_row] = lst[k];
             __threadfence();
             asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
             if (t_row == 0) {
@@ -268,17 +298,20 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                         partials + ((long long)m_tile * n_splits + sp) * kMaxK * BM);
                     for (int k = 0; k < K; ++k) {
                         const uint64_t e = __ldcg(other + k * BM + t_row);
-                        if (e > lst[(K - 1) * BM + t_row]) list_insert(lst, t_row, K, e);
+                        if (e > lst[KC - 1]) reg_insert(lst, e);
                     }
                 }
                 write_final = true;
             }
         }
         if (write_final && row < M) {
-            for (int k = 0; k < K; ++k) {
-                const uint64_t e = lst[k * BM + t_row];
-                cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
-                unary[row * K + k] = processed(key_value((uint32_t)(e >> 32)), softcap, scale);
+#pragma unroll
+            for (int k = 0; k < KC; ++k) {
+                if (k < K) {
+                    const uint64_t e = lst[k];
+                    cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
+                    unary[row * K + k] = processed(key_value((uint32_t)(e >> 32)), softcap, scale);
+                }
             }
         }
     }
@@ -347,15 +380,19 @@ cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, co
                                const uint16_t* lm_head, int M, int H, int V, int K, float softcap,
                                float scale, int32_t* cand_ids, float* unary, void* workspace,
                                uint32_t* status_word, cudaStream_t stream) {
-    static std::once_flag once[64];
-    static cudaError_t attr_err[64];
+    static std::once_flag once[3][64];
+    static cudaError_t attr_err[3][64];
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    // The register list holds KC >= K entries: the smallest build of 8, 16 or 32.
+    const int kc = K <= 8 ? 0 : (K <= 16 ? 1 : 2);
+    auto kernel = kc == 0 ? lmhead_topk_kernel<8> : (kc == 1 ? lmhead_topk_kernel<16>
+                                                              : lmhead_topk_kernel<32>);
     const size_t smem = 1024 + lm_smem_layout().total;
-    std::call_once(once[dev.device], [&] {
-        attr_err[dev.device] = cudaFuncSetAttribute(
-            lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    std::call_once(once[kc][dev.device], [&] {
+        attr_err[kc][dev.device] = cudaFuncSetAttribute(
+            kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
-    if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
+    if (attr_err[kc][dev.device] != cudaSuccess) return attr_err[kc][dev.device];
     CUtensorMap map_a, map_b;
     if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
         !encode_2d(&map_b, lm_head, (uint64_t)V, (uint64_t)H, BN))
@@ -364,7 +401,7 @@ cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, co
     uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + plan.counter_bytes);
     cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
     if (err != cudaSuccess) return err;
-    lmhead_topk_kernel<<<plan.m_tiles * plan.n_splits, kThreads, smem, stream>>>(
+    kernel<<<plan.m_tiles * plan.n_splits, kThreads, smem, stream>>>(
         map_a, map_b, M, H, V, K, plan.n_tiles, plan.n_splits, softcap, scale, cand_ids, unary,
         counters, partials, status_word);
     return cudaGetLastError();

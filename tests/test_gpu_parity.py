@@ -423,6 +423,8 @@ def _bf16(t):
     (130, 520, 8000, 8),      # ragged rows, K and V; 32 vocabulary splits of one tile each
     (300, 256, 3000, 32),     # K = 32
     (2560, 64, 20000, 16),    # 20 row tiles, 7 splits: about 11 tiles per CTA
+    (50, 64, 200, 20),        # one vocabulary tile: no split, no merge; K between list sizes
+    (40, 128, 1500, 12),      # K between list sizes, ragged last chunk of 32 columns
 ])
 def test_lmhead_topk_valid(dev, rows, H, V, K):
     g = torch.Generator().manual_seed(rows + V)
