@@ -70,14 +70,21 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
 
 // ---------------------------------------------------------------- LM head + top-k (lmhead.cu)
 
-// How the candidate head from the LM head is cut: one CTA per (128-row tile, vocabulary
-// split); the splits of a row tile are merged by whichever CTA finishes last.
+// How the candidate head from the LM head is cut. One main CTA per (128-row tile, vocabulary
+// split). When the main CTAs leave SMs idle, helper CTAs take over the tail of every split's
+// vocabulary range: the main CTA stops at rows_per_helper / (rows_per_helper + 1) of its
+// range, and each helper walks the tails of rows_per_helper consecutive row tiles in turn.
+// The partial lists of a row tile are merged by whichever CTA finishes last.
 struct LmheadPlan {
-    int m_tiles = 0;          // ceil(rows / 128)
-    int n_tiles = 0;          // ceil(V / 256)
-    int n_splits = 0;         // vocabulary ranges per row tile
-    size_t counter_bytes = 0; // per-row-tile arrival counters, padded to 256 B
-    size_t partial_bytes = 0; // [m_tiles][n_splits][32][128] uint64 lists (0 if one split)
+    int m_tiles = 0;           // ceil(rows / 128)
+    int n_tiles = 0;           // ceil(V / 256)
+    int n_splits = 0;          // vocabulary ranges per row tile
+    int rows_per_helper = 0;   // row tiles per helper CTA (0: no helpers)
+    int helpers_per_split = 0; // ceil(m_tiles / rows_per_helper), or 0
+    int slots = 0;             // partial lists per row tile: n_splits, doubled with helpers
+    int blocks = 0;            // CTAs launched
+    size_t counter_bytes = 0;  // per-row-tile arrival counters, padded to 256 B
+    size_t partial_bytes = 0;  // [m_tiles][slots][32][128] uint64 lists (0 if one slot)
     size_t workspace_bytes() const { return counter_bytes + partial_bytes; }
 };
 

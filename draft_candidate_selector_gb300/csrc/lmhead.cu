@@ -24,9 +24,13 @@
 //     spends as many steps as its busiest row has survivors. Each survivor goes into the
 //     row's sorted list, held in registers (KC = 8, 16 or 32 entries, the smallest that holds
 //     K) and updated by a branch-free network of min/max steps.
-// When a CTA has finished its range, it writes its lists to the workspace. The CTA of a row
-// tile that arrives last merges all of them and writes the K candidates. Nobody waits on
-// another CTA. Every mbarrier wait is bounded (about a second); on expiry the CTA sets
+// When the main CTAs (row tiles x splits) leave SMs idle, helper CTAs fill them: every main
+// CTA stops early in its vocabulary range, and each helper takes the remaining tails of a few
+// consecutive row tiles, one after the other. The helpers of a split walk the same vocabulary
+// tiles at the same time, as the main CTAs do, so L2 still serves each LM-head tile to many.
+// When a CTA has finished a row tile's range, it writes its lists to the workspace. The CTA
+// of a row tile that arrives last merges all of them and writes the K candidates. Nobody
+// waits on another CTA. Every mbarrier wait is bounded (about a second); on expiry the CTA sets
 // kStatusTimeout and stops.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -48,6 +52,8 @@ constexpr int kMaxK = 32;
 constexpr uint32_t kATile = BM * BK * 2;     // 16 KB
 constexpr uint32_t kBTile = BN * BK * 2;     // 32 KB
 constexpr uint32_t kTmemCols = 2 * BN;       // two accumulators
+constexpr int kMinHelperTiles = 8;           // vocabulary tiles per split before helpers pay
+constexpr int kMaxHelperRows = 16;           // row tiles per helper, at most
 
 __device__ __forceinline__ uint32_t order_key(uint32_t bits) {
     bits = (bits == 0x80000000u) ? 0u : bits;
@@ -112,8 +118,8 @@ __device__ __forceinline__ uint32_t pick32(const uint32_t (&v)[32], int j) {
 template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   int M, int H, int V, int K, int n_tiles, int n_splits, float softcap,
-                   float scale, int32_t* __restrict__ cand_ids, float* __restrict__ unary,
+                   int M, int H, int V, int K, int m_tiles, int n_tiles, int n_splits,
+                   int rows_per_helper, int helpers_per_split, float softcap, float scale, int32_t* __restrict__ cand_ids, float* __restrict__ unary,
                    uint32_t* __restrict__ counters, uint64_t* __restrict__ partials,
                    uint32_t* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
@@ -130,11 +136,32 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.x / n_splits;
-    const int split = blockIdx.x % n_splits;
-    const int n_begin = (int)((long long)split * n_tiles / n_splits);
-    const int n_end = (int)((long long)(split + 1) * n_tiles / n_splits);
-    const int T = n_end - n_begin;                       // vocabulary tiles of this CTA
+    // This CTA's work: n_seg row tiles (segments), each over the vocabulary tiles
+    // [n_begin, n_end). A main CTA has one segment, the head of its split's range. A helper
+    // has the tails of the same split for rows_per_helper consecutive row tiles.
+    const int mains = m_tiles * n_splits;
+    const bool helper = (int)blockIdx.x >= mains;
+    int split, m_first, n_seg;
+    if (!helper) {
+        m_first = blockIdx.x / n_splits;
+        split = blockIdx.x % n_splits;
+        n_seg = 1;
+    } else {
+        const int hb = blockIdx.x - mains;
+        split = hb / helpers_per_split;
+        m_first = (hb % helpers_per_split) * rows_per_helper;
+        n_seg = min(rows_per_helper, m_tiles - m_first);
+    }
+    const int s_begin = (int)((long long)split * n_tiles / n_splits);
+    const int s_end = (int)((long long)(split + 1) * n_tiles / n_splits);
+    const int cut = rows_per_helper > 0
+                        ? s_begin + (s_end - s_begin) * rows_per_helper / (rows_per_helper + 1)
+                        : s_end;
+    const int n_begin = helper ? cut : s_begin;
+    const int n_end = helper ? s_end : cut;
+    const int T = n_end - n_begin;                       // vocabulary tiles per segment
+    const int slots = rows_per_helper > 0 ? 2 * n_splits : n_splits;
+    const int slot = helper ? n_splits + split : split;  // this CTA's partial-list slot
     const int num_kb = (H + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -168,8 +195,9 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             // ---- TMA producer
             long long g = 0;
             bool ok = true;
-            for (int t = 0; t < T && ok; ++t) {
-                const int n0 = (n_begin + t) * BN;
+            for (int tt = 0; tt < n_seg * T && ok; ++tt) {
+                const int m_tile = m_first + tt / T;
+                const int n0 = (n_begin + tt % T) * BN;
                 for (int kb = 0; kb < num_kb; ++kb, ++g) {
                     const int s = (int)(g % kStages);
                     if (g >= kStages &&
@@ -195,10 +223,10 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             const uint32_t idesc = f16_idesc(BM, BN);
             long long g = 0;
             bool ok = true;
-            for (int t = 0; t < T && ok; ++t) {
-                const int buf = t & 1;
-                if (t >= 2 &&
-                    !mbar_wait(smem_u32(&tempty[buf]), (uint32_t)(((t >> 1) - 1) & 1))) {
+            for (int tt = 0; tt < n_seg * T && ok; ++tt) {
+                const int buf = tt & 1;
+                if (tt >= 2 &&
+                    !mbar_wait(smem_u32(&tempty[buf]), (uint32_t)(((tt >> 1) - 1) & 1))) {
                     atomicOr(status, kStatusTimeout);
                     break;
                 }
@@ -227,90 +255,96 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         // ---- epilogue: thread = row (tensor-memory lane) of the tile
         const int quad = warp & 3;                       // lanes 32*quad .. 32*quad + 31
         const int t_row = quad * 32 + lane;              // 0..127
-        uint64_t lst[KC];                                // descending; 0 is below every entry
-#pragma unroll
-        for (int k = 0; k < KC; ++k) lst[k] = 0;
-        float thr_f = __uint_as_float(0xFFFFFFFFu);      // NaN: everything passes at first
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
-            const int buf = t & 1;
-            const bool ready = __all_sync(0xffffffffu,
-                                          mbar_wait(smem_u32(&tfull[buf]), (uint32_t)((t >> 1) & 1)));
-            if (!ready) {
-                if (lane == 0) atomicOr(status, kStatusTimeout);
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t n0 = (uint32_t)(n_begin + t) * BN;
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                __syncwarp();
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c0), v);
-                // A value equal to the threshold cannot enter: ids arrive in ascending order,
-                // so it ties with the KC-th entry and loses on the id. NaN passes (exact
-                // order in the key), and so does everything while the list has free slots.
-                uint32_t pass = 0;
+        for (int sg = 0; sg < n_seg; ++sg) {
+            const int m_tile = m_first + sg;
+            uint64_t lst[KC];                            // descending; 0 is below every entry
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    pass |= (__uint_as_float(v[j]) <= thr_f ? 0u : 1u) << j;
-                const uint32_t id0 = n0 + (uint32_t)c0;
-                if (id0 + 32u > (uint32_t)V)                 // the zero-filled tail past V
-                    pass &= (id0 >= (uint32_t)V) ? 0u : ((1u << ((uint32_t)V - id0)) - 1u);
-                while (pass) {
-                    const int j = __ffs(pass) - 1;
-                    pass &= pass - 1;
-                    const uint64_t e = ((uint64_t)order_key(pick32(v, j)) << 32) |
-                                       (uint32_t)(~(id0 + (uint32_t)j));
-                    if (e > lst[KC - 1]) reg_insert(lst, e);
+            for (int k = 0; k < KC; ++k) lst[k] = 0;
+            float thr_f = __uint_as_float(0xFFFFFFFFu);  // NaN: everything passes at first
+            for (int t = 0; t < T && ok; ++t) {
+                const int tt = sg * T + t;
+                const int buf = tt & 1;
+                const bool ready = __all_sync(
+                    0xffffffffu, mbar_wait(smem_u32(&tfull[buf]), (uint32_t)((tt >> 1) & 1)));
+                if (!ready) {
+                    if (lane == 0) atomicOr(status, kStatusTimeout);
+                    ok = false;
+                    break;
                 }
-                thr_f = key_value((uint32_t)(lst[KC - 1] >> 32));
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&tempty[buf]));
-        }
-
-        // ---- this CTA's lists -> final candidates, or partials merged by the last CTA.
-        // Every CTA's own top K holds all of the row's top K that fall in its range, so the
-        // merge of the partial top-K lists is exact.
-        const long long row = (long long)m_tile * BM + t_row;
-        bool write_final = ok && n_splits == 1;
-        if (n_splits > 1) {
-            // The named barriers run in every epilogue thread, even after a timeout, so no
-            // thread can be left waiting at one. A CTA that timed out still arrives; its
-            // lists are then wrong, and the status word says so.
-            uint64_t* mine = partials + ((long long)m_tile * n_splits + split) * kMaxK * BM;
+                tc_fence_after();
+                const uint32_t n0 = (uint32_t)(n_begin + t) * BN;
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c0), v);
+                    // A value equal to the threshold cannot enter: ids arrive in ascending
+                    // order, so it ties with the KC-th entry and loses on the id. NaN passes
+                    // (exact order in the key), and so does everything while the list has
+                    // free slots.
+                    uint32_t pass = 0;
 #pragma unroll
-            for (int k = 0; k < KC; ++k)
-                if (k < K) mine[k * BM + t_row] = lst[k];
-            __threadfence();
-            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-            if (t_row == 0) {
-                const unsigned arrived = atomicAdd(&counters[m_tile], 1u);
-                *merge_flag = (arrived == (unsigned)(n_splits - 1)) ? 1 : 0;
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (*merge_flag) {
-                __threadfence();
-                for (int sp = 0; sp < n_splits; ++sp) {
-                    if (sp == split) continue;
-                    const unsigned long long* other = reinterpret_cast<const unsigned long long*>(
-                        partials + ((long long)m_tile * n_splits + sp) * kMaxK * BM);
-                    for (int k = 0; k < K; ++k) {
-                        const uint64_t e = __ldcg(other + k * BM + t_row);
+                    for (int j = 0; j < 32; ++j)
+                        pass |= (__uint_as_float(v[j]) <= thr_f ? 0u : 1u) << j;
+                    const uint32_t id0 = n0 + (uint32_t)c0;
+                    if (id0 + 32u > (uint32_t)V)             // the zero-filled tail past V
+                        pass &= (id0 >= (uint32_t)V) ? 0u : ((1u << ((uint32_t)V - id0)) - 1u);
+                    while (pass) {
+                        const int j = __ffs(pass) - 1;
+                        pass &= pass - 1;
+                        const uint64_t e = ((uint64_t)order_key(pick32(v, j)) << 32) |
+                                           (uint32_t)(~(id0 + (uint32_t)j));
                         if (e > lst[KC - 1]) reg_insert(lst, e);
                     }
+                    thr_f = key_value((uint32_t)(lst[KC - 1] >> 32));
                 }
-                write_final = true;
+                tc_fence_before();
+                mbar_arrive(smem_u32(&tempty[buf]));
             }
-        }
-        if (write_final && row < M) {
+
+            // ---- this segment's lists -> final candidates, or partials merged by the last
+            // CTA of the row tile. Every CTA's own top K holds all of the row's top K that fall
+            // in its range, so the merge of the partial top-K lists is exact.
+            const long long row = (long long)m_tile * BM + t_row;
+            bool write_final = ok && slots == 1;
+            if (slots > 1) {
+                // The named barriers run in every epilogue thread for every segment, even after
+                // a timeout, so no thread can be left waiting at one. A CTA that timed out
+                // still arrives; its lists are then wrong, and the status word says so.
+                uint64_t* mine = partials + ((long long)m_tile * slots + slot) * kMaxK * BM;
 #pragma unroll
-            for (int k = 0; k < KC; ++k) {
-                if (k < K) {
-                    const uint64_t e = lst[k];
-                    cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
-                    unary[row * K + k] = processed(key_value((uint32_t)(e >> 32)), softcap, scale);
+                for (int k = 0; k < KC; ++k)
+                    if (k < K) mine[k * BM + t_row] = lst[k];
+                __threadfence();
+                asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+                if (t_row == 0) {
+                    const unsigned arrived = atomicAdd(&counters[m_tile], 1u);
+                    *merge_flag = (arrived == (unsigned)(slots - 1)) ? 1 : 0;
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (*merge_flag) {
+                    __threadfence();
+                    for (int sp = 0; sp < slots; ++sp) {
+                        if (sp == slot) continue;
+                        const unsigned long long* other = reinterpret_cast<const unsigned long long*>(
+                            partials + ((long long)m_tile * slots + sp) * kMaxK * BM);
+                        for (int k = 0; k < K; ++k) {
+                            const uint64_t e = __ldcg(other + k * BM + t_row);
+                            if (e > lst[KC - 1]) reg_insert(lst, e);
+                        }
+                    }
+                    write_final = true;
+                }
+            }
+            if (write_final && row < M) {
+#pragma unroll
+                for (int k = 0; k < KC; ++k) {
+                    if (k < K) {
+                        const uint64_t e = lst[k];
+                        cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
+                        unary[row * K + k] =
+                            processed(key_value((uint32_t)(e >> 32)), softcap, scale);
+                    }
                 }
             }
         }
@@ -370,9 +404,24 @@ LmheadPlan lmhead_plan(const DeviceInfo& dev, long long rows, int V) {
     // GB300, this beat every other split count tried (1 to 38), also the ones that fill all
     // SMs in two waves: with every SM on the tensor cores the clock drops under the power
     // cap, and a second wave restarts the pipelines.
-    p.n_splits = std::max(1, std::min(p.n_tiles, std::max(1, dev.sm_count) / std::max(1, p.m_tiles)));
+    const int sms = std::max(1, dev.sm_count);
+    p.n_splits = std::max(1, std::min(p.n_tiles, sms / std::max(1, p.m_tiles)));
+    // Helpers for the SMs the main CTAs leave idle (gemma-like shapes: 60 row tiles x 2 splits
+    // leave 32 of 152). Only when each split is long enough to cut, and a helper's row count
+    // is small enough for the cut to pay.
+    const int spare = p.m_tiles <= sms ? sms - p.m_tiles * p.n_splits : 0;
+    const int g_max = spare / p.n_splits;
+    if (g_max > 0 && p.n_tiles / p.n_splits >= kMinHelperTiles) {
+        const int r = (p.m_tiles + g_max - 1) / g_max;
+        if (r <= kMaxHelperRows) {
+            p.rows_per_helper = r;
+            p.helpers_per_split = (p.m_tiles + r - 1) / r;
+        }
+    }
+    p.slots = p.rows_per_helper > 0 ? 2 * p.n_splits : p.n_splits;
+    p.blocks = p.m_tiles * p.n_splits + p.n_splits * p.helpers_per_split;
     p.counter_bytes = (size_t)((p.m_tiles * 4 + 255) / 256 * 256);
-    p.partial_bytes = p.n_splits > 1 ? (size_t)p.m_tiles * p.n_splits * kMaxK * BM * 8 : 0;
+    p.partial_bytes = p.slots > 1 ? (size_t)p.m_tiles * p.slots * kMaxK * BM * 8 : 0;
     return p;
 }
 
@@ -401,9 +450,9 @@ cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, co
     uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + plan.counter_bytes);
     cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
     if (err != cudaSuccess) return err;
-    kernel<<<plan.m_tiles * plan.n_splits, kThreads, smem, stream>>>(
-        map_a, map_b, M, H, V, K, plan.n_tiles, plan.n_splits, softcap, scale, cand_ids, unary,
-        counters, partials, status_word);
+    kernel<<<plan.blocks, kThreads, smem, stream>>>(
+        map_a, map_b, M, H, V, K, plan.m_tiles, plan.n_tiles, plan.n_splits, plan.rows_per_helper,
+        plan.helpers_per_split, softcap, scale, cand_ids, unary, counters, partials, status_word);
     return cudaGetLastError();
 }
 

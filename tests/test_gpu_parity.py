@@ -425,6 +425,10 @@ def _bf16(t):
     (2560, 64, 20000, 16),    # 20 row tiles, 7 splits: about 11 tiles per CTA
     (50, 64, 200, 20),        # one vocabulary tile: no split, no merge; K between list sizes
     (40, 128, 1500, 12),      # K between list sizes, ragged last chunk of 32 columns
+    # On 152 SMs: 40 row tiles x 3 splits plus 30 helper CTAs (4 row tiles' tails each)
+    (5000, 64, 6000, 8),
+    # On 152 SMs: 100 row tiles x 1 split plus 50 helpers (2 tails each): two lists per row
+    (12700, 64, 2100, 32),
 ])
 def test_lmhead_topk_valid(dev, rows, H, V, K):
     g = torch.Generator().manual_seed(rows + V)
