@@ -418,7 +418,9 @@ def run_lmhead(args, w: wl.Workload) -> None:
     Inputs: the workload's hidden states as the drafter's final hidden state, and a seeded
     synthetic LM head [V, H] bf16 ~ N(0, 1/sqrt(H)) drawn on the device. For context, the
     unfused route is timed too: a cuBLAS bf16 GEMM writing the logits, then this library's
-    top-k over them (fp32 logits of the same shape).
+    top-k over them (fp32 logits of the same shape). Last, the whole draft step from the LM
+    head (dflash_selector_lmhead: projection, LM-head top-k, edges) with seeded synthetic
+    projection weights and codebooks of the workload's rank.
     """
     import draft_candidate_selector_gb300 as ds
     dev = torch.device("cuda", dist_env()[2])
@@ -456,6 +458,17 @@ def run_lmhead(args, w: wl.Workload) -> None:
     logits = torch.empty((w.R, w.S, w.V), dtype=torch.float32, device=dev).normal_()
     topk_ms = timed(lambda: ds.dflash_topk_candidates(logits, w.K, cand, unary), max(3, args.steps // 4))
     del logits
+    # The whole draft step from the LM head (projection, LM-head top-k, edges) in one call.
+    w_proj = (torch.randn((w.rank, w.H), generator=g, device=dev) / w.H ** 0.5).to(torch.bfloat16)
+    pred_cb = (torch.randn((w.V, w.rank), generator=g, device=dev) / w.rank ** 0.5).to(torch.bfloat16)
+    succ_cb = (torch.randn((w.V, w.rank), generator=g, device=dev) / w.rank ** 0.5).to(torch.bfloat16)
+    anchors = torch.randint(0, w.V, (w.R,), generator=g, device=dev, dtype=torch.int32)
+    h_out = torch.empty((w.R, w.S, w.rank), dtype=torch.bfloat16, device=dev)
+    edges = torch.empty((w.R, w.S, w.K, w.K), dtype=torch.float32, device=dev)
+    sel_ms = timed(lambda: ds.dflash_selector_lmhead(hidden, lm_head, w_proj, pred_cb, succ_cb,
+                                                     anchors, w.K, cand, unary, h_out, edges, ws),
+                   max(3, args.steps // 4))
+    status |= ds.dflash_device_status(clear=True)
     flops = 2.0 * w.rows * w.V * w.H
     peak = None
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -473,6 +486,9 @@ def run_lmhead(args, w: wl.Workload) -> None:
                      "traffic": None, "peak_source": "measured sustained bf16 (MEASURED_PEAKS.json)"},
         "unfused_reference": {"cublas_bf16_gemm_ms": gemm_ms, "logits_topk_ms": topk_ms,
                               "sum_ms": gemm_ms + topk_ms},
+        "selector_lmhead": {"ms_per_step": sel_ms,
+                            "edge_scores_per_s": w.rows * w.K * w.K / (sel_ms / 1e3),
+                            "what": "projection, LM-head top-k and edges in one call"},
         "gpu_launches": args.steps, "device_status": status, "clocks": clocks.summary(),
     }), flush=True)
 

@@ -24,7 +24,7 @@ from ._native import DEVICE_BAD_ID, DEVICE_TIMEOUT, DflashError  # noqa: F401
 
 __all__ = [
     "dflash_topk_candidates", "dflash_hidden_projection", "dflash_candidate_edges",
-    "dflash_selector", "dflash_lmhead_topk", "dflash_topk_workspace_bytes",
+    "dflash_selector", "dflash_lmhead_topk", "dflash_selector_lmhead", "dflash_topk_workspace_bytes",
     "dflash_selector_workspace_bytes",
     "dflash_device_status", "dflash_trace_begin", "dflash_trace_end", "DflashError",
     "library_path",
@@ -222,6 +222,52 @@ def dflash_selector(logits: torch.Tensor, hidden: torch.Tensor, w_proj: torch.Te
     return cand_ids, unary, h_out, edges
 
 
+def dflash_selector_lmhead(hidden: torch.Tensor, lm_head: torch.Tensor, w_proj: torch.Tensor,
+                           pred_cb: torch.Tensor, succ_cb: torch.Tensor, anchors: torch.Tensor,
+                           K: int, cand_ids: torch.Tensor | None = None,
+                           unary: torch.Tensor | None = None, h_out: torch.Tensor | None = None,
+                           edges: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None,
+                           softcap: float = 0.0, scale: float = 1.0):
+    """The draft step from the LM head in one library call: returns (cand_ids, unary, h, edges).
+
+    The candidates come straight from hidden [R, S, H] . lm_head [V, H]^T, as in
+    dflash_lmhead_topk; no logits are written.
+    """
+    lib = _native.load()
+    if hidden.dim() != 3 or lm_head.dim() != 2:
+        raise ValueError("hidden must be [R, S, H] and lm_head [V, H]")
+    R, S, H = hidden.shape
+    V = lm_head.shape[0]
+    rank = w_proj.shape[0]
+    _need(hidden, "hidden", torch.bfloat16)
+    _need(lm_head, "lm_head", torch.bfloat16, (V, H))
+    _need(w_proj, "w_proj", torch.bfloat16, (rank, H))
+    _need(pred_cb, "pred_cb", torch.bfloat16, (V, rank))
+    _need(succ_cb, "succ_cb", torch.bfloat16, (V, rank))
+    _need(anchors, "anchors", torch.int32, (R,))
+    dev = hidden.device
+    with torch.cuda.device(dev):
+        if cand_ids is None:
+            cand_ids = torch.empty((R, S, K), dtype=torch.int32, device=dev)
+        if unary is None:
+            unary = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+        if h_out is None:
+            h_out = torch.empty((R, S, rank), dtype=torch.bfloat16, device=dev)
+        if edges is None:
+            edges = torch.empty((R, S, K, K), dtype=torch.float32, device=dev)
+        _need(cand_ids, "cand_ids", torch.int32, (R, S, K))
+        _need(unary, "unary", torch.float32, (R, S, K))
+        _need(h_out, "h_out", torch.bfloat16, (R, S, rank))
+        _need(edges, "edges", torch.float32, (R, S, K, K))
+        ws = _workspace(lib.dflash_selector_lmhead_workspace_bytes(R, S, V, K), dev, workspace)
+        _native.check(lib.dflash_selector_lmhead(
+            _ptr(hidden), _ptr(lm_head), _ptr(w_proj), _ptr(pred_cb), _ptr(succ_cb),
+            _ptr(anchors), R, S, K, V, H, rank, float(softcap), float(scale), _ptr(cand_ids),
+            _ptr(unary), _ptr(h_out), _ptr(edges), _ptr(ws), ws.numel(), _stream(dev, stream)))
+    return cand_ids, unary, h_out, edges
+
+
 def dflash_device_status(clear: bool = True) -> int:
     """DEVICE_* bits set by kernels on the current device since the last clear."""
     flags = ctypes.c_uint32(0)
@@ -230,7 +276,7 @@ def dflash_device_status(clear: bool = True) -> int:
 
 
 def dflash_trace_begin(n_calls: int) -> None:
-    """Record stage timing events for the next n_calls dflash_selector calls."""
+    """Record stage timing events for the next n_calls dflash_selector(_lmhead) calls."""
     _native.check(_native.load().dflash_trace_begin(int(n_calls)))
 
 

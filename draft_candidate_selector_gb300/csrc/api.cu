@@ -392,6 +392,58 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     return ok();
 }
 
+size_t dflash_selector_lmhead_workspace_bytes(int R, int S, int V, int K) {
+    return dflash_lmhead_topk_workspace_bytes(R, S, V, K);
+}
+
+dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_head,
+                                     const uint16_t* w_proj, const uint16_t* pred_cb,
+                                     const uint16_t* succ_cb, const int32_t* anchors, int R,
+                                     int S, int K, int V, int H, int rank, float softcap,
+                                     float scale, int32_t* cand_ids, float* unary,
+                                     uint16_t* h_out, float* edges, void* workspace,
+                                     size_t workspace_bytes, dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_topk(R, S, V, K));
+    DFLASH_TRY(check_processor(softcap, scale));
+    DFLASH_TRY(check_dims_projection(R, S, H, rank));
+    DFLASH_TRY(check_ptr(hidden, "hidden"));
+    DFLASH_TRY(check_ptr(lm_head, "lm_head"));
+    DFLASH_TRY(check_ptr(w_proj, "w_proj"));
+    DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
+    DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
+    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr(h_out, "h_out"));
+    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr(workspace, "workspace"));
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    const dflash::LmheadPlan plan = dflash::lmhead_plan(dev, (long long)R * S, V);
+    if (workspace_bytes < plan.workspace_bytes())
+        return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
+                    workspace_bytes, plan.workspace_bytes());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaEvent_t* ev = trace_slot(dev.device);
+    // One stream: the LM-head top-k sizes its grid to one CTA per SM, and a projection CTA
+    // beside it would push one of them into a second wave.
+    cudaError_t e;
+    if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_lmhead_topk(dev, plan, hidden, lm_head, R * S, H, V, K, softcap, scale,
+                                   cand_ids, unary, workspace, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "LM-head top-k launch");
+    if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
+                             rank, edges, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "edges launch");
+    if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    return ok();
+}
+
 dflash_status dflash_device_status(uint32_t* flags, int clear) {
     if (!flags) return fail(DFLASH_INVALID_ARGUMENT, "flags is NULL");
     DFLASH_TRY(current_device(nullptr, nullptr));

@@ -199,6 +199,36 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden,
                               void* workspace, size_t workspace_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * The draft step from the LM head: steps 1 to 3 in one call, with step 1 taken straight
+ * from the LM head as in dflash_lmhead_topk, so no logits are ever written.
+ * Source: DFlash2BeamForCausalLM.compute_candidates takes the candidates from
+ * get_top_k_tokens(lm_head, hidden, top_k), and the selector's forward scores them with the
+ * same hidden states (DFlash2BeamCandidateSelector.forward).
+ *
+ * hidden, lm_head, H, softcap, scale, cand_ids, unary   as in dflash_lmhead_topk
+ * w_proj, pred_cb, succ_cb, anchors, rank, h_out, edges as in dflash_selector
+ * workspace  at least dflash_selector_lmhead_workspace_bytes(R, S, V, K) bytes; its contents
+ *            on entry do not matter.
+ *
+ * The kernels run one after another on `stream`: projection, LM-head top-k, edges. The
+ * LM-head top-k holds one CTA on every SM, so nothing runs beside it. The call returns once
+ * everything is enqueued. The candidates may differ from an exact computation only where two
+ * logits differ by less than their fp32 accumulation error (see dflash_lmhead_topk); the edge
+ * scores are those of the candidates returned. Requires the ranges of dflash_selector and
+ * H a multiple of 8. A traced call (dflash_trace_begin) records the same four events; its
+ * top-k time counts from the start and so includes the projection.
+ * ---------------------------------------------------------------------------------- */
+size_t dflash_selector_lmhead_workspace_bytes(int R, int S, int V, int K);
+
+dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_head,
+                                     const uint16_t* w_proj, const uint16_t* pred_cb,
+                                     const uint16_t* succ_cb, const int32_t* anchors, int R,
+                                     int S, int K, int V, int H, int rank, float softcap,
+                                     float scale, int32_t* cand_ids, float* unary,
+                                     uint16_t* h_out, float* edges, void* workspace,
+                                     size_t workspace_bytes, dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Device status word. Reads the DFLASH_DEVICE_* bits that kernels on the current device
  * have set since the last clear. Clears them if `clear` is non-zero. Synchronises the
  * device. `flags` is a host pointer.
@@ -206,8 +236,8 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden,
 dflash_status dflash_device_status(uint32_t* flags, int clear);
 
 /* ------------------------------------------------------------------------------------
- * Stage tracing for dflash_selector. There is no counterpart on the pages; this is a
- * profiling aid.
+ * Stage tracing for dflash_selector and dflash_selector_lmhead. There is no counterpart on
+ * the pages; this is a profiling aid.
  * dflash_trace_begin(n) creates 4 timing events for each of the next n selector calls
  * made from this process on the current device. Each traced call records them: at its
  * start, when the projection is done (side stream), when the top-k is done and when the

@@ -132,3 +132,21 @@ def test_lmhead_argument_checks(lib):
     assert f(A, A, 2, 3, 64, 4, 8, 0.0, 1.0, A, A, A, 1 << 20, None) == _native.DFLASH_INVALID_ARGUMENT
     assert f(A, MIS, 2, 3, 64, 1000, 8, 0.0, 1.0, A, A, A, 1 << 20, None) == _native.DFLASH_INVALID_ARGUMENT
     assert f(A, A, 2, 3, 64, 1000, 8, 0.0, -1.0, A, A, A, 1 << 20, None) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_selector_lmhead_argument_checks(lib):
+    f = lib.dflash_selector_lmhead
+
+    def call(R=2, S=3, K=4, V=100, H=64, rank=16, cap=0.0, scale=1.0, ptrs=None, ws=1 << 20):
+        ptrs = ptrs or [A] * 6
+        return f(*ptrs, R, S, K, V, H, rank, cap, scale, A, A, A, A, A, ws, None)
+
+    assert call(K=33) == _native.DFLASH_UNSUPPORTED
+    assert call(H=12) == _native.DFLASH_UNSUPPORTED
+    assert call(rank=20) == _native.DFLASH_UNSUPPORTED
+    assert call(V=2, K=4) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(R=0) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(ptrs=[A, MIS, A, A, A, A]) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(ptrs=[A, A, A, A, A, P(None)]) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(scale=-2.0) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(cap=float("nan")) == _native.DFLASH_INVALID_ARGUMENT

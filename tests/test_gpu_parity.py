@@ -469,6 +469,36 @@ def test_lmhead_topk_logits_processor(dev):
                           "lm head with soft cap", softcap=5.0, scale=0.5)
 
 
+@pytest.mark.parametrize("R,S,K,V,H,rank,cap,scale", [
+    (3, 7, 8, 5000, 256, 64, 0.0, 1.0),        # 21 rows, 20 vocabulary splits
+    (40, 15, 32, 6000, 128, 128, 30.0, 1.5),   # 600 rows in 5 row tiles, K = 32, processed
+])
+def test_selector_lmhead(dev, R, S, K, V, H, rank, cap, scale):
+    """The draft step from the LM head: its candidates are those of dflash_lmhead_topk (same
+    kernel, bit for bit) and valid against the exact logits; h and the edge scores of the
+    returned candidates match the oracle."""
+    g = torch.Generator().manual_seed(R * V + K)
+    hid = _bf16(torch.randn(R, S, H, generator=g))
+    lm = _bf16(torch.randn(V, H, generator=g) / H ** 0.5)
+    wp = _bf16(torch.randn(rank, H, generator=g) / H ** 0.5)
+    pc = _bf16(torch.randn(V, rank, generator=g) / rank ** 0.5)
+    sc = _bf16(torch.randn(V, rank, generator=g) / rank ** 0.5)
+    anchors = torch.randint(0, V, (R,), generator=g, dtype=torch.int32)
+    d = [x.to(dev) for x in (hid, lm, wp, pc, sc, anchors)]
+    ids, un, h, e = ds.dflash_selector_lmhead(*d, K, softcap=cap, scale=scale)
+    ids2, un2 = ds.dflash_lmhead_topk(d[0], d[1], K, softcap=cap, scale=scale)
+    torch.cuda.synchronize(dev)
+    ids_np, un_np = ids.cpu().numpy(), un.cpu().numpy()
+    P.assert_ids_equal(ids_np, ids2.cpu().numpy(), "ids against dflash_lmhead_topk")
+    assert np.array_equal(un_np.view(np.uint32), un2.cpu().numpy().view(np.uint32))
+    P.assert_lmhead_valid(ids_np, un_np, P.bits(hid), P.bits(lm), K, "selector from the LM head",
+                          softcap=cap, scale=scale)
+    P.assert_projection(P.bits(h), P.bits(hid), P.bits(wp), "selector from the LM head: h")
+    ref_e = oracle.edges(P.bits(pc), P.bits(sc), ids_np, un_np, P.bits(h), anchors.numpy())
+    P.assert_close(e.cpu().numpy(), ref_e, "selector from the LM head: edges")
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- robustness
 
 def test_topk_fuzz_shapes(dev):
