@@ -53,7 +53,8 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, what: str) -> None:
     assert np.array_equal(np.isnan(gpu), nan_ref), f"{what}: NaN positions differ"
     g, r = gpu[~nan_ref], ref[~nan_ref]
     same_inf = (g == r)
-    err = np.where(same_inf, 0.0, np.abs(g - r))
+    with np.errstate(invalid="ignore"):      # inf - inf where both are the same infinity
+        err = np.where(same_inf, 0.0, np.abs(g - r))
     bound = RTOL * (1.0 + np.abs(r))
     bad = ~(err <= bound)
     if bad.any():
