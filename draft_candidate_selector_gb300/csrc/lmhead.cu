@@ -115,6 +115,126 @@ __device__ __forceinline__ uint32_t pick32(const uint32_t (&v)[32], int j) {
     return (j & 16) ? a[1] : a[0];
 }
 
+// The work of one CTA: n_seg row tiles (segments) from m_first on, each over the vocabulary
+// tiles [n_begin, n_begin + T). A main CTA has one segment, the head of its split's range. A
+// helper has the tails of the same split for rows_per_helper consecutive row tiles.
+struct Work {
+    int m_first, n_seg, n_begin, T, slots, slot;
+};
+
+__device__ __forceinline__ Work work_of(int w, int m_tiles, int n_tiles, int n_splits,
+                                        int rows_per_helper, int helpers_per_split) {
+    Work k;
+    const int mains = m_tiles * n_splits;
+    const bool helper = w >= mains;
+    int split;
+    if (!helper) {
+        k.m_first = w / n_splits;
+        split = w % n_splits;
+        k.n_seg = 1;
+    } else {
+        const int hb = w - mains;
+        split = hb / helpers_per_split;
+        k.m_first = (hb % helpers_per_split) * rows_per_helper;
+        k.n_seg = min(rows_per_helper, m_tiles - k.m_first);
+    }
+    const int s_begin = (int)((long long)split * n_tiles / n_splits);
+    const int s_end = (int)((long long)(split + 1) * n_tiles / n_splits);
+    const int cut = rows_per_helper > 0
+                        ? s_begin + (s_end - s_begin) * rows_per_helper / (rows_per_helper + 1)
+                        : s_end;
+    k.n_begin = helper ? cut : s_begin;
+    k.T = helper ? s_end - cut : cut - s_begin;
+    k.slots = rows_per_helper > 0 ? 2 * n_splits : n_splits;
+    k.slot = helper ? n_splits + split : split;    // this CTA's partial-list slot
+    return k;
+}
+
+// One accumulator tile into this thread's row list: the row's 256 logits of the tile are
+// read from tensor memory at taddr, 32 columns at a time; ids are n0 + column.
+template <int KC>
+__device__ __forceinline__ void scan_tile(uint32_t taddr, uint32_t n0, int V, uint64_t (&lst)[KC],
+                                          float& thr_f) {
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(taddr + (uint32_t)c0, v);
+        // A value equal to the threshold cannot enter: ids arrive in ascending order, so it
+        // ties with the KC-th entry and loses on the id. NaN passes (exact order in the key),
+        // and so does everything while the list has free slots.
+        uint32_t pass = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            pass |= (__uint_as_float(v[j]) <= thr_f ? 0u : 1u) << j;
+        const uint32_t id0 = n0 + (uint32_t)c0;
+        if (id0 + 32u > (uint32_t)V)                 // the zero-filled tail past V
+            pass &= (id0 >= (uint32_t)V) ? 0u : ((1u << ((uint32_t)V - id0)) - 1u);
+        while (pass) {
+            const int j = __ffs(pass) - 1;
+            pass &= pass - 1;
+            const uint64_t e = ((uint64_t)order_key(pick32(v, j)) << 32) |
+                               (uint32_t)(~(id0 + (uint32_t)j));
+            if (e > lst[KC - 1]) reg_insert(lst, e);
+        }
+        thr_f = key_value((uint32_t)(lst[KC - 1] >> 32));
+    }
+}
+
+// A segment's row lists (one per epilogue thread, 128 rows of 128-row tile m_tile) ->
+// final candidates, or a partial list in the workspace, merged by the last CTA of the row
+// tile to arrive. Every CTA's own top K holds all of the row's top K that fall in its range,
+// so the merge of the partial top-K lists is exact. Called by all four epilogue
+// warps together: the named barriers run in every epilogue thread for every segment, even
+// after a timeout, so no thread is left waiting at one. A CTA that timed out still arrives;
+// its lists are then wrong, and the status word says so.
+template <int KC>
+__device__ __forceinline__ void finish_segment(uint64_t (&lst)[KC], bool ok, int m_tile,
+                                               int slots, int slot, int t_row, int M, int K,
+                                               float softcap, float scale, int* merge_flag,
+                                               int32_t* __restrict__ cand_ids,
+                                               float* __restrict__ unary,
+                                               uint32_t* __restrict__ counters,
+                                               uint64_t* __restrict__ partials) {
+    const long long row = (long long)m_tile * BM + t_row;
+    bool write_final = ok && slots == 1;
+    if (slots > 1) {
+        uint64_t* mine = partials + ((long long)m_tile * slots + slot) * kMaxK * BM;
+#pragma unroll
+        for (int k = 0; k < KC; ++k)
+            if (k < K) mine[k * BM + t_row] = lst[k];
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+        if (t_row == 0) {
+            const unsigned arrived = atomicAdd(&counters[m_tile], 1u);
+            *merge_flag = (arrived == (unsigned)(slots - 1)) ? 1 : 0;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*merge_flag) {
+            __threadfence();
+            for (int sp = 0; sp < slots; ++sp) {
+                if (sp == slot) continue;
+                const unsigned long long* other = reinterpret_cast<const unsigned long long*>(
+                    partials + ((long long)m_tile * slots + sp) * kMaxK * BM);
+                for (int k = 0; k < K; ++k) {
+                    const uint64_t e = __ldcg(other + k * BM + t_row);
+                    if (e > lst[KC - 1]) reg_insert(lst, e);
+                }
+            }
+            write_final = true;
+        }
+    }
+    if (write_final && row < M) {
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            if (k < K) {
+                const uint64_t e = lst[k];
+                cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
+                unary[row * K + k] = processed(key_value((uint32_t)(e >> 32)), softcap, scale);
+            }
+        }
+    }
+}
+
 template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -136,32 +256,9 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // This CTA's work: n_seg row tiles (segments), each over the vocabulary tiles
-    // [n_begin, n_end). A main CTA has one segment, the head of its split's range. A helper
-    // has the tails of the same split for rows_per_helper consecutive row tiles.
-    const int mains = m_tiles * n_splits;
-    const bool helper = (int)blockIdx.x >= mains;
-    int split, m_first, n_seg;
-    if (!helper) {
-        m_first = blockIdx.x / n_splits;
-        split = blockIdx.x % n_splits;
-        n_seg = 1;
-    } else {
-        const int hb = blockIdx.x - mains;
-        split = hb / helpers_per_split;
-        m_first = (hb % helpers_per_split) * rows_per_helper;
-        n_seg = min(rows_per_helper, m_tiles - m_first);
-    }
-    const int s_begin = (int)((long long)split * n_tiles / n_splits);
-    const int s_end = (int)((long long)(split + 1) * n_tiles / n_splits);
-    const int cut = rows_per_helper > 0
-                        ? s_begin + (s_end - s_begin) * rows_per_helper / (rows_per_helper + 1)
-                        : s_end;
-    const int n_begin = helper ? cut : s_begin;
-    const int n_end = helper ? s_end : cut;
-    const int T = n_end - n_begin;                       // vocabulary tiles per segment
-    const int slots = rows_per_helper > 0 ? 2 * n_splits : n_splits;
-    const int slot = helper ? n_splits + split : split;  // this CTA's partial-list slot
+    const Work wk = work_of(blockIdx.x, m_tiles, n_tiles, n_splits, rows_per_helper,
+                            helpers_per_split);
+    const int m_first = wk.m_first, n_seg = wk.n_seg, n_begin = wk.n_begin, T = wk.T;
     const int num_kb = (H + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -257,7 +354,6 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         const int t_row = quad * 32 + lane;              // 0..127
         bool ok = true;
         for (int sg = 0; sg < n_seg; ++sg) {
-            const int m_tile = m_first + sg;
             uint64_t lst[KC];                            // descending; 0 is below every entry
 #pragma unroll
             for (int k = 0; k < KC; ++k) lst[k] = 0;
@@ -273,80 +369,13 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     break;
                 }
                 tc_fence_after();
-                const uint32_t n0 = (uint32_t)(n_begin + t) * BN;
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t v[32];
-                    __syncwarp();
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c0), v);
-                    // A value equal to the threshold cannot enter: ids arrive in ascending
-                    // order, so it ties with the KC-th entry and loses on the id. NaN passes
-                    // (exact order in the key), and so does everything while the list has
-                    // free slots.
-                    uint32_t pass = 0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        pass |= (__uint_as_float(v[j]) <= thr_f ? 0u : 1u) << j;
-                    const uint32_t id0 = n0 + (uint32_t)c0;
-                    if (id0 + 32u > (uint32_t)V)             // the zero-filled tail past V
-                        pass &= (id0 >= (uint32_t)V) ? 0u : ((1u << ((uint32_t)V - id0)) - 1u);
-                    while (pass) {
-                        const int j = __ffs(pass) - 1;
-                        pass &= pass - 1;
-                        const uint64_t e = ((uint64_t)order_key(pick32(v, j)) << 32) |
-                                           (uint32_t)(~(id0 + (uint32_t)j));
-                        if (e > lst[KC - 1]) reg_insert(lst, e);
-                    }
-                    thr_f = key_value((uint32_t)(lst[KC - 1] >> 32));
-                }
+                scan_tile(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN),
+                          (uint32_t)(n_begin + t) * BN, V, lst, thr_f);
                 tc_fence_before();
                 mbar_arrive(smem_u32(&tempty[buf]));
             }
-
-            // ---- this segment's lists -> final candidates, or partials merged by the last
-            // CTA of the row tile. Every CTA's own top K holds all of the row's top K that fall
-            // in its range, so the merge of the partial top-K lists is exact.
-            const long long row = (long long)m_tile * BM + t_row;
-            bool write_final = ok && slots == 1;
-            if (slots > 1) {
-                // The named barriers run in every epilogue thread for every segment, even after
-                // a timeout, so no thread can be left waiting at one. A CTA that timed out
-                // still arrives; its lists are then wrong, and the status word says so.
-                uint64_t* mine = partials + ((long long)m_tile * slots + slot) * kMaxK * BM;
-#pragma unroll
-                for (int k = 0; k < KC; ++k)
-                    if (k < K) mine[k * BM + t_row] = lst[k];
-                __threadfence();
-                asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-                if (t_row == 0) {
-                    const unsigned arrived = atomicAdd(&counters[m_tile], 1u);
-                    *merge_flag = (arrived == (unsigned)(slots - 1)) ? 1 : 0;
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (*merge_flag) {
-                    __threadfence();
-                    for (int sp = 0; sp < slots; ++sp) {
-                        if (sp == slot) continue;
-                        const unsigned long long* other = reinterpret_cast<const unsigned long long*>(
-                            partials + ((long long)m_tile * slots + sp) * kMaxK * BM);
-                        for (int k = 0; k < K; ++k) {
-                            const uint64_t e = __ldcg(other + k * BM + t_row);
-                            if (e > lst[KC - 1]) reg_insert(lst, e);
-                        }
-                    }
-                    write_final = true;
-                }
-            }
-            if (write_final && row < M) {
-#pragma unroll
-                for (int k = 0; k < KC; ++k) {
-                    if (k < K) {
-                        const uint64_t e = lst[k];
-                        cand_ids[row * K + k] = (int32_t)(~(uint32_t)e);
-                        unary[row * K + k] =
-                            processed(key_value((uint32_t)(e >> 32)), softcap, scale);
-                    }
-                }
-            }
+            finish_segment(lst, ok, m_first + sg, wk.slots, wk.slot, t_row, M, K, softcap, scale,
+                           merge_flag, cand_ids, unary, counters, partials);
         }
     }
     tc_fence_before();
