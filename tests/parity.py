@@ -141,11 +141,13 @@ def assert_lmhead_valid(gpu_ids: np.ndarray, gpu_unary: np.ndarray, hidden_bits:
     """
     H = hidden_bits.shape[-1]
     V = lm_head_bits.shape[0]
-    x = bits_to_f64(hidden_bits).reshape(-1, H)
-    w = bits_to_f64(lm_head_bits).reshape(V, H)
+    ax = np.abs(bits_to_f64(hidden_bits).reshape(-1, H))
     ref_ids, _, exact = oracle.lmhead_topk(hidden_bits.reshape(-1, H), lm_head_bits, K,
                                            softcap=softcap, scale=scale, want_logits=True)
-    tol = 2.0 * H * 2.0 ** -24 * (np.abs(x) @ np.abs(w).T)
+    tol = np.empty((ax.shape[0], V))
+    for v0 in range(0, V, 4096):             # in chunks: the LM head may be gigabytes
+        aw = np.abs(bits_to_f64(lm_head_bits[v0:v0 + 4096]).reshape(-1, H))
+        tol[:, v0:v0 + aw.shape[0]] = 2.0 * H * 2.0 ** -24 * (ax @ aw.T)
     gi = np.asarray(gpu_ids).reshape(-1, K)
     gu = np.asarray(gpu_unary, dtype=np.float64).reshape(-1, K)
     same = 0

@@ -441,6 +441,27 @@ def test_lmhead_topk_valid(dev, rows, H, V, K):
     _status_clean()
 
 
+@pytest.mark.parametrize("name", ["qwen_zipf", "gemma_large"])
+def test_lmhead_topk_full_size_sampled(dev, name):
+    """At the full sizes the benchmark times, in the launch configuration it times (on 152 SMs:
+    qwen_zipf 8 row tiles x 19 splits, the last tile half padding; gemma_large 60 x 2 splits
+    plus 30 helper CTAs), sampled rows against the exact logits of the oracle."""
+    w = wl.WORKLOADS[name]
+    hid = wl._bf16_normal(0, wl._TAG_HIDDEN, (w.R, w.S, w.H), 1.0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    lm = (torch.randn((w.V, w.H), generator=g, device=dev) / w.H ** 0.5).to(torch.bfloat16)
+    ids, un = ds.dflash_lmhead_topk(hid.to(dev), lm, w.K)
+    last = w.rows - 1
+    rows = P.sample_rows(w.rows, 4, seed=11, extra=[127, 128, last - 128, last - 1])
+    ids = ids.cpu().numpy().reshape(-1, w.K)[rows]
+    un = un.cpu().numpy().reshape(-1, w.K)[rows]
+    hb = P.bits(hid).reshape(-1, w.H)[rows]
+    same = P.assert_lmhead_valid(ids, un, hb, P.bits(lm), w.K, f"{name} sampled rows")
+    assert same >= 0.5, f"only {same:.2f} of the sampled rows match the exact order"
+    _status_clean()
+
+
 def test_lmhead_topk_one_hot_exact(dev):
     """One-hot hidden states make every logit an exact LM-head entry: no rounding at all, so
     the ids must equal the oracle's, ties (planted in the LM head) included."""
