@@ -24,7 +24,8 @@ from ._native import DEVICE_BAD_ID, DEVICE_TIMEOUT, DflashError  # noqa: F401
 
 __all__ = [
     "dflash_topk_candidates", "dflash_hidden_projection", "dflash_candidate_edges",
-    "dflash_selector", "dflash_lmhead_topk", "dflash_selector_lmhead", "dflash_topk_workspace_bytes",
+    "dflash_selector", "dflash_selector_forward", "dflash_lmhead_topk", "dflash_selector_lmhead",
+    "dflash_topk_workspace_bytes",
     "dflash_selector_workspace_bytes",
     "dflash_device_status", "dflash_trace_begin", "dflash_trace_end", "DflashError",
     "library_path",
@@ -220,6 +221,43 @@ def dflash_selector(logits: torch.Tensor, hidden: torch.Tensor, w_proj: torch.Te
             _ptr(anchors), R, S, K, V, H, rank, float(softcap), float(scale), _ptr(cand_ids),
             _ptr(unary), _ptr(h_out), _ptr(edges), _ptr(ws), ws.numel(), _stream(dev, stream)))
     return cand_ids, unary, h_out, edges
+
+
+def dflash_selector_forward(cand_ids: torch.Tensor, unary: torch.Tensor, hidden: torch.Tensor,
+                            anchors: torch.Tensor, w_proj: torch.Tensor, pred_cb: torch.Tensor,
+                            succ_cb: torch.Tensor, h_out: torch.Tensor | None = None,
+                            edges: torch.Tensor | None = None, stream=None):
+    """The selector's forward pass on given candidates: returns (h, edges).
+
+    cand_ids int32 [R, S, K] and unary fp32 [R, S, K] are the candidates and their logits;
+    h = hidden . w_proj^T is computed first, then the edge scores [R, S, K, K].
+    """
+    lib = _native.load()
+    if cand_ids.dim() != 3 or hidden.dim() != 3:
+        raise ValueError("cand_ids must be [R, S, K] and hidden [R, S, H]")
+    R, S, K = cand_ids.shape
+    H = hidden.shape[2]
+    rank = w_proj.shape[0]
+    V = pred_cb.shape[0]
+    _need(cand_ids, "cand_ids", torch.int32)
+    _need(unary, "unary", torch.float32, (R, S, K))
+    _need(hidden, "hidden", torch.bfloat16, (R, S, H))
+    _need(anchors, "anchors", torch.int32, (R,))
+    _need(w_proj, "w_proj", torch.bfloat16, (rank, H))
+    _need(pred_cb, "pred_cb", torch.bfloat16, (V, rank))
+    _need(succ_cb, "succ_cb", torch.bfloat16, (V, rank))
+    dev = hidden.device
+    with torch.cuda.device(dev):
+        if h_out is None:
+            h_out = torch.empty((R, S, rank), dtype=torch.bfloat16, device=dev)
+        if edges is None:
+            edges = torch.empty((R, S, K, K), dtype=torch.float32, device=dev)
+        _need(h_out, "h_out", torch.bfloat16, (R, S, rank))
+        _need(edges, "edges", torch.float32, (R, S, K, K))
+        _native.check(lib.dflash_selector_forward(
+            _ptr(cand_ids), _ptr(unary), _ptr(hidden), _ptr(anchors), _ptr(w_proj), _ptr(pred_cb),
+            _ptr(succ_cb), R, S, K, V, H, rank, _ptr(h_out), _ptr(edges), _stream(dev, stream)))
+    return h_out, edges
 
 
 def dflash_selector_lmhead(hidden: torch.Tensor, lm_head: torch.Tensor, w_proj: torch.Tensor,

@@ -392,6 +392,35 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     return ok();
 }
 
+dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unary,
+                                      const uint16_t* hidden, const int32_t* anchors,
+                                      const uint16_t* w_proj, const uint16_t* pred_cb,
+                                      const uint16_t* succ_cb, int R, int S, int K, int V, int H,
+                                      int rank, uint16_t* h_out, float* edges,
+                                      dflash_stream_t stream) {
+    DFLASH_TRY(check_dims_edges(R, S, K, V, rank));
+    DFLASH_TRY(check_dims_projection(R, S, H, rank));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr(hidden, "hidden"));
+    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_ptr(w_proj, "w_proj"));
+    DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
+    DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
+    DFLASH_TRY(check_ptr(h_out, "h_out"));
+    DFLASH_TRY(check_ptr(edges, "edges"));
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
+                             rank, edges, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "edges launch");
+    return ok();
+}
+
 size_t dflash_selector_lmhead_workspace_bytes(int R, int S, int V, int K) {
     return dflash_lmhead_topk_workspace_bytes(R, S, V, K);
 }

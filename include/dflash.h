@@ -199,6 +199,26 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden,
                               void* workspace, size_t workspace_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * The selector's forward pass: steps 2 and 3 on candidates the caller already has.
+ * Source: DFlash2BeamCandidateSelector.forward(candidate_ids, unary_logits, hidden_states,
+ * anchor_token_ids), which scores the candidates with candidate_edges on the projected
+ * hidden states and returns the edge scores [requests, steps, top_k (predecessor), top_k].
+ *
+ * cand_ids, unary, anchors, pred_cb, succ_cb, K, V, rank, edges  as in dflash_candidate_edges
+ * hidden, w_proj, H, h_out                                      as in dflash_hidden_projection
+ *
+ * The projection writes h_out, then the edges read it; both run on `stream` and the call
+ * returns once they are enqueued. No workspace. The ranges are those of the two calls. It
+ * is not traced by dflash_trace_begin, which traces the calls that include step 1.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unary,
+                                      const uint16_t* hidden, const int32_t* anchors,
+                                      const uint16_t* w_proj, const uint16_t* pred_cb,
+                                      const uint16_t* succ_cb, int R, int S, int K, int V, int H,
+                                      int rank, uint16_t* h_out, float* edges,
+                                      dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * The draft step from the LM head: steps 1 to 3 in one call, with step 1 taken straight
  * from the LM head as in dflash_lmhead_topk, so no logits are ever written.
  * Source: DFlash2BeamForCausalLM.compute_candidates takes the candidates from

@@ -150,3 +150,21 @@ def test_selector_lmhead_argument_checks(lib):
     assert call(ptrs=[A, A, A, A, A, P(None)]) == _native.DFLASH_INVALID_ARGUMENT
     assert call(scale=-2.0) == _native.DFLASH_INVALID_ARGUMENT
     assert call(cap=float("nan")) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_selector_forward_argument_checks(lib):
+    f = lib.dflash_selector_forward
+
+    def call(R=2, S=3, K=4, V=100, H=64, rank=16, ptrs=None):
+        ptrs = ptrs or [A] * 7
+        return f(*ptrs, R, S, K, V, H, rank, A, A, None)
+
+    if not torch.cuda.is_available():
+        assert call() == _native.DFLASH_NO_DEVICE    # valid arguments reach the device check
+    assert call(K=33) == _native.DFLASH_UNSUPPORTED
+    assert call(K=8, V=4) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(H=12) == _native.DFLASH_UNSUPPORTED
+    assert call(rank=264) == _native.DFLASH_UNSUPPORTED
+    assert call(S=0) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(ptrs=[A, A, MIS, A, A, A, A]) == _native.DFLASH_INVALID_ARGUMENT
+    assert call(ptrs=[A, A, A, P(None), A, A, A]) == _native.DFLASH_INVALID_ARGUMENT

@@ -412,6 +412,36 @@ def test_selector_logits_processor(dev, name):
     _status_clean()
 
 
+@pytest.mark.parametrize("name", SMALL + ["ragged"])
+def test_selector_forward(dev, name):
+    """The selector's forward pass on given candidates. Fed the fused selector's candidates it
+    reproduces its h and edges bit for bit; fed arbitrary candidates (repeats included) its
+    h and edges match the oracle."""
+    inp = host_inputs(RAGGED if name == "ragged" else name)
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    ids, un, h, e = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                                       d["succ_cb"], d["anchors"], w.K)
+    h2, e2 = ds.dflash_selector_forward(ids, un, d["hidden"], d["anchors"], d["w_proj"],
+                                        d["pred_cb"], d["succ_cb"])
+    torch.cuda.synchronize(dev)
+    assert np.array_equal(P.bits(h2), P.bits(h))
+    assert np.array_equal(e2.cpu().numpy().view(np.uint32), e.cpu().numpy().view(np.uint32))
+
+    rng = np.random.default_rng(17)
+    cand = rng.integers(0, w.V, size=(w.R, w.S, w.K)).astype(np.int32)
+    cand[:, :, -1] = cand[:, :, 0]                    # a repeated candidate in every row
+    unary = rng.standard_normal((w.R, w.S, w.K)).astype(np.float32)
+    h3, e3 = ds.dflash_selector_forward(torch.from_numpy(cand).to(dev),
+                                        torch.from_numpy(unary).to(dev), d["hidden"],
+                                        d["anchors"], d["w_proj"], d["pred_cb"], d["succ_cb"])
+    P.assert_projection(P.bits(h3), P.bits(inp.hidden), P.bits(inp.w_proj), f"{name} forward h")
+    ref = oracle.edges(P.bits(inp.pred_cb), P.bits(inp.succ_cb), cand, unary, P.bits(h3),
+                       inp.anchors)
+    P.assert_close(e3.cpu().numpy(), ref, f"{name} forward edges")
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- candidate head from the LM head
 
 def _bf16(t):
