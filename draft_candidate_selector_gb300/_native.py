@@ -47,6 +47,7 @@ SIGNATURES = {
     "dflash_selector_lmhead": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _f, _p,
                                     _p, _p, _p, _p, _sz, _p]),
     "dflash_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
+    "dflash_selftest_wait_timeout": (_i, []),
     "dflash_trace_begin": (_i, [_i]),
     "dflash_trace_end": (_i, [ctypes.POINTER(ctypes.c_float), _i, ctypes.POINTER(ctypes.c_int)]),
 }

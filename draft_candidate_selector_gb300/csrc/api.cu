@@ -5,6 +5,7 @@
 // arithmetic of the method lives in topk.cu, projection.cu and edges.cu.
 #include "dflash.h"
 #include "common.cuh"
+#include "ptx.cuh"
 
 #include <cmath>
 #include <cstdarg>
@@ -470,6 +471,33 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
                              rank, edges, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "edges launch");
     if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    return ok();
+}
+
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives on; the bounded wait gives up.
+__global__ void wait_timeout_kernel(uint32_t* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = dflash::ptx::smem_u32(&bar);
+        dflash::ptx::mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!dflash::ptx::mbar_wait(b, 0)) atomicOr(status, dflash::kStatusTimeout);
+    }
+}
+
+}  // namespace
+
+dflash_status dflash_selftest_wait_timeout(void) {
+    dflash::DeviceInfo dev;
+    uint32_t* status = nullptr;
+    DFLASH_TRY(current_device(&dev, &status));
+    wait_timeout_kernel<<<1, 32>>>(status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "wait self-check launch");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "wait self-check");
     return ok();
 }
 

@@ -256,6 +256,16 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
 dflash_status dflash_device_status(uint32_t* flags, int clear);
 
 /* ------------------------------------------------------------------------------------
+ * Self-check of the wait limit. There is no counterpart on the pages; this is a test aid for
+ * the failure path. It launches one thread that waits on an mbarrier nothing ever arrives
+ * on, through the same bounded wait the pipelined kernels use (projection, LM-head top-k).
+ * The wait gives up after about one second, sets DFLASH_DEVICE_TIMEOUT in the status word,
+ * and the kernel returns: nothing traps or faults, and the context stays usable. Synchronises
+ * the device; read and clear the bit with dflash_device_status.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_selftest_wait_timeout(void);
+
+/* ------------------------------------------------------------------------------------
  * Stage tracing for dflash_selector and dflash_selector_lmhead. There is no counterpart on
  * the pages; this is a profiling aid.
  * dflash_trace_begin(n) creates 4 timing events for each of the next n selector calls

@@ -17,6 +17,7 @@ import torch
 import oracle
 import parity as P
 import draft_candidate_selector_gb300 as ds
+from draft_candidate_selector_gb300 import _native
 from draft_candidate_selector_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -547,6 +548,23 @@ def test_selector_lmhead(dev, R, S, K, V, H, rank, cap, scale):
     P.assert_projection(P.bits(h), P.bits(hid), P.bits(wp), "selector from the LM head: h")
     ref_e = oracle.edges(P.bits(pc), P.bits(sc), ids_np, un_np, P.bits(h), anchors.numpy())
     P.assert_close(e.cpu().numpy(), ref_e, "selector from the LM head: edges")
+    _status_clean()
+
+
+def test_wait_timeout_is_reported_and_the_context_survives(dev):
+    """The failure path of the bounded waits, without a fault: a wait on an mbarrier that
+    nothing arrives on gives up after about a second and sets the timeout bit; afterwards the
+    same context still runs the top-k correctly."""
+    import time
+    lib = _native.load()
+    ds.dflash_device_status(clear=True)
+    t0 = time.perf_counter()
+    _native.check(lib.dflash_selftest_wait_timeout())
+    dt = time.perf_counter() - t0
+    assert ds.dflash_device_status(clear=True) & _native.DEVICE_TIMEOUT
+    assert 0.5 < dt < 30.0, dt
+    x = np.random.default_rng(3).standard_normal((2, 3, 5000)).astype(np.float32)
+    _topk_case(dev, x, 8, "top-k after a timeout")
     _status_clean()
 
 
