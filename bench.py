@@ -468,6 +468,18 @@ def run_lmhead(args, w: wl.Workload) -> None:
     sel_ms = timed(lambda: ds.dflash_selector_lmhead(hidden, lm_head, w_proj, pred_cb, succ_cb,
                                                      anchors, w.K, cand, unary, h_out, edges, ws),
                    max(3, args.steps // 4))
+    # End to end: each step copies its hidden states in from pinned host memory and its edge
+    # scores out (the LM head, projection and codebooks stay resident, as model weights do).
+    hidden_host = hidden.cpu().pin_memory()
+    edges_host = torch.empty(edges.shape, dtype=edges.dtype).pin_memory()
+
+    def e2e_step():
+        hidden.copy_(hidden_host, non_blocking=True)
+        ds.dflash_selector_lmhead(hidden, lm_head, w_proj, pred_cb, succ_cb, anchors, w.K, cand,
+                                  unary, h_out, edges, ws)
+        edges_host.copy_(edges, non_blocking=True)
+
+    e2e_ms = timed(e2e_step, max(3, args.steps // 4))
     status |= ds.dflash_device_status(clear=True)
     flops = 2.0 * w.rows * w.V * w.H
     peak = None
@@ -488,7 +500,11 @@ def run_lmhead(args, w: wl.Workload) -> None:
                               "sum_ms": gemm_ms + topk_ms},
         "selector_lmhead": {"ms_per_step": sel_ms,
                             "edge_scores_per_s": w.rows * w.K * w.K / (sel_ms / 1e3),
-                            "what": "projection, LM-head top-k and edges in one call"},
+                            "what": "projection, LM-head top-k and edges in one call",
+                            "e2e": {"ms_per_step": e2e_ms,
+                                    "edge_scores_per_s": w.rows * w.K * w.K / (e2e_ms / 1e3),
+                                    "h2d_bytes_per_step": hidden_host.numel() * 2,
+                                    "d2h_bytes_per_step": edges_host.numel() * 4}},
         "gpu_launches": args.steps, "device_status": status, "clocks": clocks.summary(),
     }), flush=True)
 
