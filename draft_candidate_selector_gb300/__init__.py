@@ -26,7 +26,8 @@ __all__ = [
     "dflash_topk_candidates", "dflash_hidden_projection", "dflash_candidate_edges",
     "dflash_selector", "dflash_selector_forward", "dflash_lmhead_topk", "dflash_selector_lmhead",
     "dflash_topk_workspace_bytes",
-    "dflash_selector_workspace_bytes",
+    "dflash_selector_workspace_bytes", "dflash_lmhead_topk_workspace_bytes",
+    "dflash_selector_lmhead_workspace_bytes",
     "dflash_device_status", "dflash_trace_begin", "dflash_trace_end", "DflashError",
     "library_path",
 ]
@@ -66,6 +67,14 @@ def dflash_topk_workspace_bytes(R: int, S: int, V: int, K: int) -> int:
 
 def dflash_selector_workspace_bytes(R: int, S: int, V: int, K: int) -> int:
     return int(_native.load().dflash_selector_workspace_bytes(R, S, V, K))
+
+
+def dflash_lmhead_topk_workspace_bytes(R: int, S: int, V: int, K: int) -> int:
+    return int(_native.load().dflash_lmhead_topk_workspace_bytes(R, S, V, K))
+
+
+def dflash_selector_lmhead_workspace_bytes(R: int, S: int, V: int, K: int) -> int:
+    return int(_native.load().dflash_selector_lmhead_workspace_bytes(R, S, V, K))
 
 
 def _workspace(nbytes: int, dev: torch.device, workspace: torch.Tensor | None) -> torch.Tensor:

@@ -209,7 +209,8 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden,
  *
  * The projection writes h_out, then the edges read it; both run on `stream` and the call
  * returns once they are enqueued. No workspace. The ranges are those of the two calls. It
- * is not traced by dflash_trace_begin, which traces the calls that include step 1.
+ * is not traced by dflash_trace_begin, which traces the calls that include step 1. It can be
+ * captured in a CUDA graph; make one call on the device before capturing.
  * ---------------------------------------------------------------------------------- */
 dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unary,
                                       const uint16_t* hidden, const int32_t* anchors,
@@ -236,7 +237,9 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
  * logits differ by less than their fp32 accumulation error (see dflash_lmhead_topk); the edge
  * scores are those of the candidates returned. Requires the ranges of dflash_selector and
  * H a multiple of 8. A traced call (dflash_trace_begin) records the same four events; its
- * top-k time counts from the start and so includes the projection.
+ * top-k time counts from the start and so includes the projection. It can be captured in a
+ * CUDA graph; make one call on the device before capturing (the first call sets the kernels'
+ * shared-memory limits).
  * ---------------------------------------------------------------------------------- */
 size_t dflash_selector_lmhead_workspace_bytes(int R, int S, int V, int K);
 

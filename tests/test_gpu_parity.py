@@ -568,6 +568,60 @@ def test_wait_timeout_is_reported_and_the_context_survives(dev):
     _status_clean()
 
 
+@pytest.mark.parametrize("entry", ["selector_lmhead", "selector_forward"])
+def test_draft_step_cuda_graph_replay(dev, entry):
+    """The draft step captured once in a CUDA graph and replayed on fresh inputs copied into
+    the captured buffers gives, bit for bit, what eager calls give."""
+    R, S, K, V, H, rank = 6, 7, 16, 5000, 256, 64
+    g = torch.Generator().manual_seed(77)
+    lm = _bf16(torch.randn(V, H, generator=g) / H ** 0.5).to(dev)
+    wp = _bf16(torch.randn(rank, H, generator=g) / H ** 0.5).to(dev)
+    pc = _bf16(torch.randn(V, rank, generator=g) / rank ** 0.5).to(dev)
+    sc = _bf16(torch.randn(V, rank, generator=g) / rank ** 0.5).to(dev)
+    hid = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
+    anchors = torch.empty((R,), dtype=torch.int32, device=dev)
+    cand = torch.empty((R, S, K), dtype=torch.int32, device=dev)
+    unary = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+    h = torch.empty((R, S, rank), dtype=torch.bfloat16, device=dev)
+    edges = torch.empty((R, S, K, K), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.dflash_selector_lmhead_workspace_bytes(R, S, V, K), dtype=torch.uint8,
+                     device=dev)
+
+    def fresh(seed):
+        gg = torch.Generator().manual_seed(seed)
+        hid.copy_(_bf16(torch.randn(R, S, H, generator=gg)))
+        anchors.copy_(torch.randint(0, V, (R,), generator=gg, dtype=torch.int32))
+        cand.copy_(torch.randint(0, V, (R, S, K), generator=gg, dtype=torch.int32))
+        unary.copy_(torch.randn(R, S, K, generator=gg))
+
+    def call():
+        if entry == "selector_lmhead":
+            ds.dflash_selector_lmhead(hid, lm, wp, pc, sc, anchors, K, cand, unary, h, edges, ws)
+        else:
+            ds.dflash_selector_forward(cand, unary, hid, anchors, wp, pc, sc, h, edges)
+
+    fresh(0)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        call()                                       # eager warm-up on a side stream
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for seed in (1, 2):
+        fresh(seed)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        got = [x.clone() for x in (cand, unary, h, edges)]
+        fresh(seed)
+        call()
+        torch.cuda.synchronize(dev)
+        for a, b in zip(got, (cand, unary, h, edges)):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"{entry} replay {seed}"
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- robustness
 
 def test_topk_fuzz_shapes(dev):
