@@ -7,6 +7,8 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -168,6 +170,16 @@ dflash_status check_ptr(const void* p, const char* name) {
         if (_s != DFLASH_OK) return _s;      \
     } while (0)
 
+// A named NVTX range around one library call (host side: it brackets the argument checks and
+// the enqueue, and profilers attach the call's CUDA launches to it). Free when no tool is
+// attached.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // ---------------------------------------------------------------- stage tracing
 
 struct Trace {
@@ -222,6 +234,7 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
                                      float softcap, float scale, int32_t* cand_ids,
                                      float* unary, void* workspace, size_t workspace_bytes,
                                      dflash_stream_t stream) {
+    NvtxRange range("dflash_topk_candidates");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_ptr(logits, "logits"));
@@ -243,6 +256,7 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
 dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, int V, int K,
                                              int32_t* cand_ids, float* unary,
                                              dflash_stream_t stream) {
+    NvtxRange range("dflash_topk_candidates_noalloc");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_ptr(logits, "logits"));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
@@ -276,6 +290,7 @@ dflash_status dflash_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head
                                  int H, int V, int K, float softcap, float scale,
                                  int32_t* cand_ids, float* unary, void* workspace,
                                  size_t workspace_bytes, dflash_stream_t stream) {
+    NvtxRange range("dflash_lmhead_topk");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
     if (H < 1) return fail(DFLASH_INVALID_ARGUMENT, "H=%d must be >= 1", H);
@@ -302,6 +317,7 @@ dflash_status dflash_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head
 dflash_status dflash_hidden_projection(const uint16_t* hidden, const uint16_t* w_proj, int R,
                                        int S, int H, int rank, uint16_t* h_out,
                                        dflash_stream_t stream) {
+    NvtxRange range("dflash_hidden_projection");
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
     DFLASH_TRY(check_ptr(hidden, "hidden"));
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
@@ -320,6 +336,7 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
                                      const uint16_t* h, const int32_t* anchors, int R, int S,
                                      int K, int V, int rank, float* edges,
                                      dflash_stream_t stream) {
+    NvtxRange range("dflash_candidate_edges");
     DFLASH_TRY(check_dims_edges(R, S, K, V, rank));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
@@ -344,6 +361,7 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
                               float softcap, float scale, int32_t* cand_ids, float* unary,
                               uint16_t* h_out, float* edges, void* workspace,
                               size_t workspace_bytes, dflash_stream_t stream) {
+    NvtxRange range("dflash_selector");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
@@ -399,6 +417,7 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
                                       const uint16_t* succ_cb, int R, int S, int K, int V, int H,
                                       int rank, uint16_t* h_out, float* edges,
                                       dflash_stream_t stream) {
+    NvtxRange range("dflash_selector_forward");
     DFLASH_TRY(check_dims_edges(R, S, K, V, rank));
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
@@ -433,6 +452,7 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
                                      float scale, int32_t* cand_ids, float* unary,
                                      uint16_t* h_out, float* edges, void* workspace,
                                      size_t workspace_bytes, dflash_stream_t stream) {
+    NvtxRange range("dflash_selector_lmhead");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
