@@ -237,9 +237,11 @@ __device__ __forceinline__ void finish_segment(uint64_t (&lst)[KC], bool ok, int
 
 template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
-lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   int M, int H, int V, int K, int m_tiles, int n_tiles, int n_splits,
-                   int rows_per_helper, int helpers_per_split, float softcap, float scale, int32_t* __restrict__ cand_ids, float* __restrict__ unary,
+lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, int M, int H, int V, int K,
+                   int m_tiles, int n_tiles, int n_splits, int rows_per_helper,
+                   int helpers_per_split, float softcap, float scale,
+                   int32_t* __restrict__ cand_ids, float* __restrict__ unary,
                    uint32_t* __restrict__ counters, uint64_t* __restrict__ partials,
                    uint32_t* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
