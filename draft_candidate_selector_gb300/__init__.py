@@ -25,6 +25,7 @@ from ._native import DEVICE_BAD_ID, DEVICE_TIMEOUT, DflashError  # noqa: F401
 __all__ = [
     "dflash_topk_candidates", "dflash_hidden_projection", "dflash_candidate_edges",
     "dflash_selector", "dflash_selector_forward", "dflash_lmhead_topk", "dflash_selector_lmhead",
+    "dflash_best_path",
     "dflash_topk_workspace_bytes",
     "dflash_selector_workspace_bytes", "dflash_lmhead_topk_workspace_bytes",
     "dflash_selector_lmhead_workspace_bytes",
@@ -313,6 +314,33 @@ def dflash_selector_lmhead(hidden: torch.Tensor, lm_head: torch.Tensor, w_proj: 
             _ptr(anchors), R, S, K, V, H, rank, float(softcap), float(scale), _ptr(cand_ids),
             _ptr(unary), _ptr(h_out), _ptr(edges), _ptr(ws), ws.numel(), _stream(dev, stream)))
     return cand_ids, unary, h_out, edges
+
+
+def dflash_best_path(edges: torch.Tensor, cand_ids: torch.Tensor, path: torch.Tensor | None = None,
+                     tokens: torch.Tensor | None = None, score: torch.Tensor | None = None,
+                     stream=None):
+    """Max-sum path through edge scores [R, S, K, K]: returns (path int32 [R, S],
+    tokens int32 [R, S], score fp32 [R])."""
+    lib = _native.load()
+    if edges.dim() != 4 or edges.shape[2] != edges.shape[3]:
+        raise ValueError("edges must be [R, S, K, K]")
+    R, S, K, _ = edges.shape
+    _need(edges, "edges", torch.float32)
+    _need(cand_ids, "cand_ids", torch.int32, (R, S, K))
+    dev = edges.device
+    with torch.cuda.device(dev):
+        if path is None:
+            path = torch.empty((R, S), dtype=torch.int32, device=dev)
+        if tokens is None:
+            tokens = torch.empty((R, S), dtype=torch.int32, device=dev)
+        if score is None:
+            score = torch.empty((R,), dtype=torch.float32, device=dev)
+        _need(path, "path", torch.int32, (R, S))
+        _need(tokens, "tokens", torch.int32, (R, S))
+        _need(score, "score", torch.float32, (R,))
+        _native.check(lib.dflash_best_path(_ptr(edges), _ptr(cand_ids), R, S, K, _ptr(path),
+                                           _ptr(tokens), _ptr(score), _stream(dev, stream)))
+    return path, tokens, score
 
 
 def dflash_device_status(clear: bool = True) -> int:

@@ -43,6 +43,7 @@ SIGNATURES = {
                              _p, _p, _p, _sz, _p]),
     "dflash_selector_forward": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p,
                                      _p]),
+    "dflash_best_path": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p]),
     "dflash_selector_lmhead_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "dflash_selector_lmhead": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _f, _p,
                                     _p, _p, _p, _p, _sz, _p]),

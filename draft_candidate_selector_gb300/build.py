@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(OUT_DIR, "libdflash_gb300.so")
-SOURCES = ["api.cu", "topk.cu", "projection.cu", "edges.cu", "lmhead.cu"]
+SOURCES = ["api.cu", "topk.cu", "projection.cu", "edges.cu", "lmhead.cu", "path.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -441,6 +441,29 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
     return ok();
 }
 
+dflash_status dflash_best_path(const float* edges, const int32_t* cand_ids, int R, int S, int K,
+                               int32_t* path, int32_t* tokens, float* score,
+                               dflash_stream_t stream) {
+    NvtxRange range("dflash_best_path");
+    if (R < 1 || S < 1 || K < 1)
+        return fail(DFLASH_INVALID_ARGUMENT, "R, S and K must be >= 1 (got R=%d S=%d K=%d)", R, S,
+                    K);
+    if (K > 32) return fail(DFLASH_UNSUPPORTED, "K=%d: the best path supports K <= 32", K);
+    if (S > dflash::kMaxPathSteps)
+        return fail(DFLASH_UNSUPPORTED, "S=%d: the best path supports S <= %d", S,
+                    dflash::kMaxPathSteps);
+    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr(path, "path"));
+    DFLASH_TRY(check_ptr(tokens, "tokens"));
+    DFLASH_TRY(check_ptr(score, "score"));
+    DFLASH_TRY(current_device(nullptr, nullptr));
+    cudaError_t e = dflash::launch_best_path(edges, cand_ids, R, S, K, path, tokens, score,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "best path launch");
+    return ok();
+}
+
 size_t dflash_selector_lmhead_workspace_bytes(int R, int S, int V, int K) {
     return dflash_lmhead_topk_workspace_bytes(R, S, V, K);
 }

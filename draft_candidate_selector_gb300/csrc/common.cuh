@@ -95,4 +95,12 @@ cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, co
                                float scale, int32_t* cand_ids, float* unary, void* workspace,
                                uint32_t* status_word, cudaStream_t stream);
 
+// ---------------------------------------------------------------- best path (path.cu)
+
+constexpr int kMaxPathSteps = 256;   // steps per request the best path supports
+
+// One warp per request: the max-sum path through E [R,S,K,K] (K <= 32, S <= kMaxPathSteps).
+cudaError_t launch_best_path(const float* edges, const int32_t* cand_ids, int R, int S, int K,
+                             int32_t* path, int32_t* tokens, float* score, cudaStream_t stream);
+
 }  // namespace dflash

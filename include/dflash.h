@@ -252,6 +252,31 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
                                      size_t workspace_bytes, dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * Best path through the edge scores: one candidate per step for every request.
+ * Reading: the pages say the selector rescores each position's top-k tokens against the
+ * token before it (page "vllm.models.beam.nvidia.dflash2", module docstring) but show no
+ * consumer of the scores. This call takes the plainest one: the path that maximises the sum
+ * over p of E[r,p,c_{p-1},c_p], the predecessor row at p = 0 being q = 0 (every q row there
+ * is the anchor's).
+ *
+ * edges     [R, S, K, K] float  edge scores as dflash_candidate_edges writes them
+ * cand_ids  [R, S, K]    int32  the candidates
+ * path      [R, S]       int32  out: the chosen candidate index c_p at each step
+ * tokens    [R, S]       int32  out: cand_ids[r, p, c_p], the drafted tokens
+ * score     [R]          float  out: the path's score
+ *
+ * Max-sum dynamic programming in fp32, in a fixed order: V_0[c] = E[r,0,0,c]; V_p[c] is the
+ * running maximum over q = 0..K-1 of V_{p-1}[q] + E[r,p,q,c], replaced only by a strictly
+ * larger sum (ties keep the lower q; IEEE compares, so a NaN never replaces and is never
+ * replaced); the last candidate is the running maximum of V_{S-1}, same rule, and the path
+ * follows the kept predecessors back. The result is therefore exactly reproducible.
+ * Requires 1 <= K <= 32 and S <= 256 (DFLASH_UNSUPPORTED beyond). No workspace.
+ * ---------------------------------------------------------------------------------- */
+dflash_status dflash_best_path(const float* edges, const int32_t* cand_ids, int R, int S, int K,
+                               int32_t* path, int32_t* tokens, float* score,
+                               dflash_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Device status word. Reads the DFLASH_DEVICE_* bits that kernels on the current device
  * have set since the last clear. Clears them if `clear` is non-zero. Synchronises the
  * device. `flags` is a host pointer.

@@ -41,6 +41,8 @@ class Oracle:
         lib.oracle_lmhead_topk.argtypes = [p, p, i64, i64, i64, i32, ctypes.c_double,
                                            ctypes.c_double, p, p, p, i32]
         lib.oracle_lmhead_topk.restype = i32
+        lib.oracle_best_path.argtypes = [p, p, i64, i64, i32, p, p, p, i32]
+        lib.oracle_best_path.restype = i32
         self.lib = lib
         self.path = path
 
@@ -168,6 +170,23 @@ class Oracle:
         return ids, un, h, e
 
 
+    def best_path(self, edges: np.ndarray, cand: np.ndarray, threads: int | None = None):
+        """Max-sum path over edge scores [R, S, K, K] (fp32, the order of the C source):
+        returns (path int32 [R, S], tokens int32 [R, S], score float32 [R])."""
+        e = _c(edges, np.float32)
+        cd = _c(cand, np.int32)
+        R, S, K, K2 = e.shape
+        assert K == K2 and cd.shape == (R, S, K)
+        path = np.empty((R, S), dtype=np.int32)
+        tokens = np.empty((R, S), dtype=np.int32)
+        score = np.empty((R,), dtype=np.float32)
+        rc = self.lib.oracle_best_path(_ptr(e), _ptr(cd), R, S, K, _ptr(path), _ptr(tokens),
+                                       _ptr(score), threads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_best_path failed (rc={rc})")
+        return path, tokens, score
+
+
 _default: Oracle | None = None
 
 
@@ -218,6 +237,10 @@ def selector(logits, hidden_bits, w_bits, pred_bits, succ_bits, anchors, K, thre
              softcap=0.0, scale=1.0):
     return get().selector(logits, hidden_bits, w_bits, pred_bits, succ_bits, anchors, K,
                           threads, softcap, scale)
+
+
+def best_path(edges, cand, threads=None):
+    return get().best_path(edges, cand, threads)
 
 
 def bits_to_float(bits: np.ndarray) -> np.ndarray:

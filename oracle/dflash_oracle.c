@@ -32,6 +32,11 @@
  *   - Edges: exact (fp64) sums over the bf16 values, stored as fp32. pred*h is not
  *     rounded before the dot product.
  *
+ *   - Best path over the edge scores (what consumes E is not shown on the pages; the
+ *       reading is the max-sum path through the candidate lattice): for each request,
+ *       one candidate per step maximising the sum of E[r,p,c_{p-1},c_p], in fp32 with
+ *       the order and tie rule written at oracle_best_path below.
+ *
  * Every computation is the plain definition. Top-k fully sorts the row. The dot
  * products are single fp64 loops. Rows are split across pthreads only for wall time;
  * each row is computed exactly as in the serial loop.
@@ -360,4 +365,81 @@ int oracle_selector(const float* logits, const uint16_t* hidden, const uint16_t*
     if (rc) return rc;
     return oracle_edges(pred_cb, succ_cb, V, rank, ids, unary, h_out, anchors, R, S, K, edges,
                         threads);
+}
+
+/* ---------------------------------------------------------------------------------
+ * Best path over the edge scores. The pages say the selector rescores each step's top-k
+ * candidates against the token before it; what consumes the scores is not shown. The
+ * reading: for request r, choose one candidate index c_p per step p so that the sum over
+ * p of E[r,p,c_{p-1},c_p] is largest, the predecessor row at p = 0 being q = 0 (every q row
+ * is the anchor's there). Max-sum dynamic programming over the steps, in fp32, in this
+ * order:
+ *   V_0[c] = E[r,0,0,c];
+ *   V_p[c] = the largest of V_{p-1}[q] + E[r,p,q,c] over q = 0, 1, ..., K-1, taken as a
+ *            running maximum that a later q replaces only with a strictly larger sum (ties
+ *            keep the lower q; IEEE compares, so a NaN neither replaces nor is replaced);
+ *   c_{S-1} = the running maximum of V_{S-1}[c] over c, same rule; c_{p-1} = the q kept
+ *            for (p, c_p).
+ * Outputs: path[r,p] = c_p, tokens[r,p] = cand[r,p,c_p], score[r] = V_{S-1}[c_{S-1}].
+ * The arithmetic is fp32 on purpose: a GPU that takes the same decisions in the same
+ * precision and order gives the same path, bit for bit.
+ * --------------------------------------------------------------------------------- */
+typedef struct {
+    const float* edges;
+    const int32_t* cand;
+    int64_t S;
+    int K;
+    int32_t* path;
+    int32_t* tokens;
+    float* score;
+    int failed;
+} PathCtx;
+
+static void path_row(void* ctx, int64_t r) {
+    PathCtx* c = (PathCtx*)ctx;
+    const int K = c->K;
+    const int64_t S = c->S;
+    const float* E = c->edges + r * S * K * K;
+    float v[32] = {0}, nv[32];
+    unsigned char* keep = (unsigned char*)malloc((size_t)(S * K));
+    if (!keep) {
+        c->failed = 1;
+        return;
+    }
+    for (int j = 0; j < K; ++j) v[j] = E[j];                 /* p = 0, predecessor row q = 0 */
+    for (int64_t p = 1; p < S; ++p) {
+        const float* Ep = E + p * K * K;
+        for (int j = 0; j < K; ++j) {
+            float best = v[0] + Ep[j];
+            int bq = 0;
+            for (int q = 1; q < K; ++q) {
+                const float s = v[q] + Ep[q * K + j];
+                if (s > best) {
+                    best = s;
+                    bq = q;
+                }
+            }
+            nv[j] = best;
+            keep[p * K + j] = (unsigned char)bq;
+        }
+        memcpy(v, nv, sizeof(float) * (size_t)K);
+    }
+    int cur = 0;
+    for (int j = 1; j < K; ++j)
+        if (v[j] > v[cur]) cur = j;
+    c->score[r] = v[cur];
+    for (int64_t p = S - 1; p >= 0; --p) {
+        c->path[r * S + p] = cur;
+        c->tokens[r * S + p] = c->cand[(r * S + p) * K + cur];
+        if (p > 0) cur = keep[p * K + cur];
+    }
+    free(keep);
+}
+
+int oracle_best_path(const float* edges, const int32_t* cand, int64_t R, int64_t S, int K,
+                     int32_t* path, int32_t* tokens, float* score, int threads) {
+    if (R < 1 || S < 1 || K < 1 || K > 32) return -1;
+    PathCtx c = {edges, cand, S, K, path, tokens, score, 0};
+    parallel_rows(path_row, &c, R, threads);
+    return c.failed ? -2 : 0;
 }

@@ -431,6 +431,93 @@ def pin_lmhead_topk_one_hot(orc) -> None:
     assert ids[0].tolist() == want and np.array_equal(un[0], col[want])
 
 
+def pin_best_path_golden(orc) -> None:
+    """The hand-worked case of tests/golden/best_path_worked.txt, ties included."""
+    K = S = 0
+    entries, cands = [], []
+    for line in _golden_lines("best_path_worked.txt"):
+        tok = line.split()
+        if tok[0] == "K":
+            K = int(tok[1])
+        elif tok[0] == "S":
+            S = int(tok[1])
+        elif tok[0] == "E":
+            entries.append((int(tok[1]), int(tok[2]), int(tok[3]), float(tok[4])))
+        elif tok[0] == "cand":
+            cands.append((int(tok[1]), int(tok[2]), int(tok[3])))
+        elif tok[0] == "path":
+            want_path = [int(x) for x in tok[1:]]
+        elif tok[0] == "tokens":
+            want_tokens = [int(x) for x in tok[1:]]
+        elif tok[0] == "score":
+            want_score = float(tok[1])
+    E = np.zeros((1, S, K, K), dtype=np.float32)
+    for p_, q, c, v in entries:
+        E[0, p_, q, c] = v
+    cand = np.zeros((1, S, K), dtype=np.int32)
+    for p_, c, i in cands:
+        cand[0, p_, c] = i
+    path, tokens, score = orc.best_path(E, cand)
+    assert path[0].tolist() == want_path, path
+    assert tokens[0].tolist() == want_tokens, tokens
+    assert float(score[0]) == want_score, score
+
+
+def _path_sum(E: np.ndarray, path) -> float:
+    """Exact sum of a path's scores (p = 0 uses predecessor row 0)."""
+    s = float(E[0, 0, path[0]])
+    for p_ in range(1, len(path)):
+        s += float(E[p_, path[p_ - 1], path[p_]])
+    return s
+
+
+def pin_best_path_bruteforce(orc, trials: int = 60, seed: int = 15) -> None:
+    """Against every path on tiny lattices. Scores lie on a 1/8 grid in [-4, 4], so every
+    fp32 sum is exact: the oracle's score must equal the best path sum, and so must the sum
+    of the path it returns."""
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        S = int(rng.integers(1, 6))
+        K = int(rng.integers(1, 5))
+        R = 2
+        E = (rng.integers(-32, 33, size=(R, S, K, K)) / 8.0).astype(np.float32)
+        cand = rng.integers(0, 1000, size=(R, S, K)).astype(np.int32)
+        path, tokens, score = orc.best_path(E, cand)
+        for r in range(R):
+            best = max(_path_sum(E[r], pth) for pth in itertools.product(range(K), repeat=S))
+            assert float(score[r]) == best
+            assert _path_sum(E[r], path[r].tolist()) == best
+            assert tokens[r].tolist() == [int(cand[r, p_, path[r, p_]]) for p_ in range(S)]
+
+
+def pin_best_path_independent_steps(orc, seed: int = 16) -> None:
+    """With no pairwise term (E[p,q,c] = u[p,c] for every q, as zero codebooks give), the best
+    path takes each step's best candidate, the first one on ties, and the score is the fp32
+    sum of those, left to right."""
+    rng = np.random.default_rng(seed)
+    R, S, K = 4, 6, 8
+    u = np.round(rng.standard_normal((R, S, K)) * 4).astype(np.float32)   # ties on purpose
+    E = np.repeat(u[:, :, None, :], K, axis=2)
+    cand = np.arange(R * S * K, dtype=np.int32).reshape(R, S, K)
+    path, tokens, score = orc.best_path(E, cand)
+    for r in range(R):
+        want = [int(np.argmax(u[r, p_])) for p_ in range(S)]          # first maximum
+        assert path[r].tolist() == want
+        acc = np.float32(0)
+        for p_ in range(S):
+            acc = np.float32(acc + u[r, p_, want[p_]]) if p_ else u[r, 0, want[0]]
+        assert score[r] == acc
+
+
+def pin_best_path_single_candidate(orc) -> None:
+    """K = 1: the only path; its score is the fp32 sum of E[p,0,0], left to right."""
+    E = np.array([[[[0.5]], [[-2.25]], [[1e-3]]]], dtype=np.float32)
+    cand = np.array([[[7], [8], [9]]], dtype=np.int32)
+    path, tokens, score = orc.best_path(E, cand)
+    assert path[0].tolist() == [0, 0, 0] and tokens[0].tolist() == [7, 8, 9]
+    assert score[0] == np.float32(np.float32(np.float32(0.5) + np.float32(-2.25)) + np.float32(1e-3))
+
+
 ALL_PINS = [
     pin_topk_golden, pin_topk_bruteforce, pin_topk_stable_sort, pin_topk_invariants,
     pin_topk_logits_processor_golden, pin_topk_logits_processor_vs_numpy,
@@ -438,5 +525,6 @@ ALL_PINS = [
     pin_projection_golden, pin_projection_closed_forms, pin_projection_vs_numpy,
     pin_edges_golden, pin_edges_zero_codebooks, pin_edges_rank1, pin_edges_structure,
     pin_edges_vs_einsum, pin_selector_composes, pin_lmhead_topk_vs_numpy,
-    pin_lmhead_topk_one_hot,
+    pin_lmhead_topk_one_hot, pin_best_path_golden, pin_best_path_bruteforce,
+    pin_best_path_independent_steps, pin_best_path_single_candidate,
 ]

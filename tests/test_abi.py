@@ -168,3 +168,15 @@ def test_selector_forward_argument_checks(lib):
     assert call(S=0) == _native.DFLASH_INVALID_ARGUMENT
     assert call(ptrs=[A, A, MIS, A, A, A, A]) == _native.DFLASH_INVALID_ARGUMENT
     assert call(ptrs=[A, A, A, P(None), A, A, A]) == _native.DFLASH_INVALID_ARGUMENT
+
+
+def test_best_path_argument_checks(lib):
+    f = lib.dflash_best_path
+    assert f(A, A, 0, 3, 4, A, A, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(A, A, 2, 3, 0, A, A, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(A, A, 2, 3, 33, A, A, A, None) == _native.DFLASH_UNSUPPORTED
+    assert f(A, A, 2, 257, 4, A, A, A, None) == _native.DFLASH_UNSUPPORTED
+    assert f(MIS, A, 2, 3, 4, A, A, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(A, A, 2, 3, 4, A, P(None), A, None) == _native.DFLASH_INVALID_ARGUMENT
+    if not torch.cuda.is_available():
+        assert f(A, A, 2, 3, 4, A, A, A, None) == _native.DFLASH_NO_DEVICE

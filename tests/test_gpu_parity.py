@@ -443,6 +443,56 @@ def test_selector_forward(dev, name):
     _status_clean()
 
 
+@pytest.mark.parametrize("name", SMALL + ["ragged"] + LARGE)
+def test_best_path(dev, name):
+    """The best path through the fused selector's edge scores equals the oracle's (same fp32
+    decisions in the same order): path, tokens and score bit for bit, every request."""
+    w = wl.WORKLOADS[name] if name != "ragged" else RAGGED
+    if name in LARGE:
+        # Edge scores shaped like the workload's, without the (large) logits: the path only
+        # reads E and the candidates.
+        rng = np.random.default_rng(31)
+        e = rng.standard_normal((w.R, w.S, w.K, w.K)).astype(np.float32)
+        cand = rng.integers(0, w.V, size=(w.R, w.S, w.K)).astype(np.int32)
+        E = torch.from_numpy(e).to(dev)
+        ids = torch.from_numpy(cand).to(dev)
+    else:
+        inp = host_inputs(RAGGED if name == "ragged" else name)
+        d = P.to_device(inp, dev)
+        ids, _, _, E = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                                          d["succ_cb"], d["anchors"], w.K)
+    path, tokens, score = ds.dflash_best_path(E, ids)
+    ref_path, ref_tokens, ref_score = oracle.best_path(E.cpu().numpy(), ids.cpu().numpy())
+    P.assert_ids_equal(path.cpu().numpy(), ref_path, f"{name} path")
+    P.assert_ids_equal(tokens.cpu().numpy(), ref_tokens, f"{name} tokens")
+    assert np.array_equal(score.cpu().numpy().view(np.uint32), ref_score.view(np.uint32))
+    _status_clean()
+
+
+def test_best_path_ties_and_edge_shapes(dev):
+    """Exact ties everywhere (integer scores), K = 1, odd K and K = 32, S = 1 and the maximum
+    S, and NaNs and infinities: every choice must match the oracle's scan exactly."""
+    rng = np.random.default_rng(32)
+    for (R, S, K) in [(5, 7, 4), (3, 1, 8), (4, 9, 1), (2, 256, 32), (9, 15, 32), (6, 11, 7),
+                      (8, 15, 32)]:
+        e = rng.integers(-2, 3, size=(R, S, K, K)).astype(np.float32)      # many ties
+        if K == 32 and S == 15 and R == 8:
+            # NaNs (as bad candidate ids give) and infinities, at predecessor 0 and elsewhere
+            e[rng.random(e.shape) < 0.05] = np.nan
+            e[rng.random(e.shape) < 0.02] = np.inf
+            e[rng.random(e.shape) < 0.02] = -np.inf
+            e[0, 3, 0, :] = np.nan
+        cand = rng.integers(0, 1 << 20, size=(R, S, K)).astype(np.int32)
+        path, tokens, score = ds.dflash_best_path(torch.from_numpy(e).to(dev),
+                                                  torch.from_numpy(cand).to(dev))
+        rp, rt, rs = oracle.best_path(e, cand)
+        P.assert_ids_equal(path.cpu().numpy(), rp, f"path R={R} S={S} K={K}")
+        P.assert_ids_equal(tokens.cpu().numpy(), rt, f"tokens R={R} S={S} K={K}")
+        # Equal values; a NaN score matches a NaN (its payload is the adder's, not the data's)
+        assert np.array_equal(score.cpu().numpy(), rs, equal_nan=True)
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- candidate head from the LM head
 
 def _bf16(t):

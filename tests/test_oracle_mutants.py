@@ -94,6 +94,24 @@ MUTANTS = [
     ("edges_h_dropped",
      "s += bf16_to_double(a[j]) * bf16_to_double(hp[j]) * bf16_to_double(b[j]);",
      "s += bf16_to_double(a[j]) * bf16_to_double(b[j]);"),
+    ("best_path_ties_to_higher_predecessor",
+     "if (s > best) {",
+     "if (s >= best) {"),
+    ("best_path_final_tie_to_higher",
+     "if (v[j] > v[cur]) cur = j;",
+     "if (v[j] >= v[cur]) cur = j;"),
+    ("best_path_first_step_diagonal_row",
+     "for (int j = 0; j < K; ++j) v[j] = E[j];",
+     "for (int j = 0; j < K; ++j) v[j] = E[j * K + j];"),
+    ("best_path_predecessor_not_kept",
+     "keep[p * K + j] = (unsigned char)bq;",
+     "keep[p * K + j] = (unsigned char)0;"),
+    ("best_path_transposed_scores",
+     "const float s = v[q] + Ep[q * K + j];",
+     "const float s = v[q] + Ep[j * K + q];"),
+    ("best_path_tokens_from_previous_step",
+     "c->tokens[r * S + p] = c->cand[(r * S + p) * K + cur];",
+     "c->tokens[r * S + p] = c->cand[(r * S + (p > 0 ? p - 1 : p)) * K + cur];"),
 ]
 
 
