@@ -145,7 +145,7 @@ class ClockSampler:
     def summary(self) -> dict | None:
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -157,6 +157,10 @@ class ClockSampler:
                     smax.append(float(parts[2]))
                 except ValueError:
                     continue
+                try:
+                    power.append(float(parts[3]))
+                except ValueError:
+                    pass
                 for n, v in zip(names, parts[5:]):
                     if v.lower() == "active":
                         reasons.add(n)
@@ -164,6 +168,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w": statistics.median(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -468,6 +473,38 @@ def run_lmhead(args, w: wl.Workload) -> None:
     sel_ms = timed(lambda: ds.dflash_selector_lmhead(hidden, lm_head, w_proj, pred_cb, succ_cb,
                                                      anchors, w.K, cand, unary, h_out, edges, ws),
                    max(3, args.steps // 4))
+    sustained = None
+    if args.sustained:
+        # Each of the fused kernel and the cuBLAS GEMM alone, back to back for about
+        # args.sustained seconds with clocks sampled: under the power cap the clock settles
+        # where the power allows, so work per cycle decides the rate.
+        sustained = {}
+        h2 = hidden.reshape(w.rows, w.H)
+        for name, fn in [("lmhead_topk_kernel", step),
+                         ("cublas_bf16_gemm", lambda: torch.matmul(h2, lm_head.t()))]:
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            n = max(5, int(args.sustained * 1e3 / max(a.elapsed_time(b), 1e-3)))
+            with ClockSampler(dev) as ck:
+                a.record(stream)
+                for _ in range(n):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+            s_ms = a.elapsed_time(b) / n
+            ck_s = ck.summary() or {}
+            tflops = 2.0 * w.rows * w.V * w.H / (s_ms / 1e3) / 1e12
+            mhz = ck_s.get("sm_mhz")
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            sustained[name] = {
+                "ms": s_ms, "tflops": tflops, "calls": n, "clocks": ck_s,
+                "flop_per_sm_cycle": tflops * 1e12 / (sms * mhz * 1e6) if mhz else None}
     # End to end: each step copies its hidden states in from pinned host memory and its edge
     # scores out (the LM head, projection and codebooks stay resident, as model weights do).
     hidden_host = hidden.cpu().pin_memory()
@@ -505,6 +542,7 @@ def run_lmhead(args, w: wl.Workload) -> None:
                                     "edge_scores_per_s": w.rows * w.K * w.K / (e2e_ms / 1e3),
                                     "h2d_bytes_per_step": hidden_host.numel() * 2,
                                     "d2h_bytes_per_step": edges_host.numel() * 4}},
+        "sustained": sustained,
         "gpu_launches": args.steps, "device_status": status, "clocks": clocks.summary(),
     }), flush=True)
 
@@ -573,6 +611,9 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lmhead", action="store_true",
                     help="time the candidate head straight from a synthetic LM head instead")
+    ap.add_argument("--sustained", type=float, default=0.0,
+                    help="with --lmhead: also run the fused kernel and the cuBLAS GEMM back to "
+                         "back for this many seconds each, sampling clocks and power")
     ap.add_argument("--best-path", action="store_true",
                     help="time the best path through edge scores of the workload's shape instead")
     ap.add_argument("--path-steps", type=int, default=None,
