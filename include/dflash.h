@@ -11,6 +11,10 @@
  *      E[r,p,q,c] = unary[r,p,c] + <pred_cb[cand[r,p-1,q]] * h_p, succ_cb[cand[r,p,c]]>,
  *      where the predecessor at p = 0 is the request's anchor token.
  *                                        DFlash2BeamCandidateSelector (class docstring)
+ * Around these: step 1 straight from the LM head without logits in memory
+ * (dflash_lmhead_topk, dflash_selector_lmhead), steps 2 and 3 on given candidates
+ * (dflash_selector_forward), and the best path through E (dflash_best_path, a reading: the
+ * page does not show what consumes E).
  *
  * Conventions for every entry point:
  *   - Pointers are caller-owned DEVICE memory on the current CUDA device, unless a
@@ -19,9 +23,10 @@
  *   - Every pointer must be 16-byte aligned (vector loads and TMA), or the call returns
  *     DFLASH_INVALID_ARGUMENT.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream). They
- *     allocate no device memory and do not synchronise the device. A non-OK status
- *     means nothing was launched, except DFLASH_CUDA_ERROR, which reports a launch
- *     failure.
+ *     allocate no device memory and do not synchronise the device; dflash_device_status,
+ *     dflash_trace_end and dflash_selftest_wait_timeout are the exceptions, and say so. A
+ *     non-OK status means nothing was launched, except DFLASH_CUDA_ERROR, which reports a
+ *     launch failure.
  *   - Supported sizes: R, S >= 1; 1 <= K <= 32 and K <= V; V < 2^31; H a multiple of 8;
  *     rank a multiple of 8 in [8, 256]. Out-of-range sizes give DFLASH_INVALID_ARGUMENT
  *     (bad values) or DFLASH_UNSUPPORTED (valid but not implemented, for example K > 32).
