@@ -164,6 +164,15 @@ dflash_status check_ptr(const void* p, const char* name) {
     return DFLASH_OK;
 }
 
+// The anchors are read one id at a time, so their natural 4-byte alignment suffices (a slice
+// of requests out of a larger anchors array stays valid).
+dflash_status check_anchors(const int32_t* p) {
+    if (!p) return fail(DFLASH_INVALID_ARGUMENT, "anchors is NULL");
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0)
+        return fail(DFLASH_INVALID_ARGUMENT, "anchors is not 4-byte aligned");
+    return DFLASH_OK;
+}
+
 #define DFLASH_TRY(expr)                     \
     do {                                     \
         dflash_status _s = (expr);           \
@@ -343,7 +352,7 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(h, "h"));
-    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_anchors(anchors));
     DFLASH_TRY(check_ptr(edges, "edges"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
@@ -370,7 +379,7 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
-    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_anchors(anchors));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));
@@ -423,7 +432,7 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(hidden, "hidden"));
-    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_anchors(anchors));
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
@@ -484,7 +493,7 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
-    DFLASH_TRY(check_ptr(anchors, "anchors"));
+    DFLASH_TRY(check_anchors(anchors));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));

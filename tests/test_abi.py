@@ -180,3 +180,16 @@ def test_best_path_argument_checks(lib):
     assert f(A, A, 2, 3, 4, A, P(None), A, None) == _native.DFLASH_INVALID_ARGUMENT
     if not torch.cuda.is_available():
         assert f(A, A, 2, 3, 4, A, A, A, None) == _native.DFLASH_NO_DEVICE
+
+
+def test_anchors_need_only_natural_alignment(lib):
+    """anchors is read one id at a time: 4-byte alignment passes the checks, 2-byte does not."""
+    f = lib.dflash_candidate_edges
+    ok4, bad2 = P(4096 + 4), P(4096 + 2)
+    expect_ok = _native.DFLASH_NO_DEVICE if not torch.cuda.is_available() else None
+    st = f(A, A, A, A, A, ok4, 2, 3, 4, 100, 16, A, None)
+    assert st != _native.DFLASH_INVALID_ARGUMENT or b"anchors" not in lib.dflash_last_error()
+    if expect_ok is not None:
+        assert st == expect_ok
+    assert f(A, A, A, A, A, bad2, 2, 3, 4, 100, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert b"anchors" in lib.dflash_last_error()

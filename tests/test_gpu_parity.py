@@ -672,6 +672,33 @@ def test_draft_step_cuda_graph_replay(dev, entry):
     _status_clean()
 
 
+@pytest.mark.parametrize("name", ["small_ties", "ragged"])
+def test_selector_request_chunks_equal_one_call(dev, name):
+    """The end-to-end benchmark runs the fused selector on request chunks. Every kernel's
+    per-row arithmetic is independent of how many rows a call holds, so chunked calls must
+    give exactly the results of one call."""
+    inp = host_inputs(RAGGED if name == "ragged" else name)
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    whole = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                               d["succ_cb"], d["anchors"], w.K)
+    cuts = [0, 1, w.R // 2, w.R] if w.R > 2 else [0, 1, w.R]
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if a == b:
+            continue
+        # Copies of the logits and hidden slices (16-byte aligned, as the header asks; with
+        # V % 4 != 0 a slice of the logits is not). The anchors slice is a plain view.
+        parts.append(ds.dflash_selector(d["logits"][a:b].clone(), d["hidden"][a:b].clone(),
+                                        d["w_proj"], d["pred_cb"], d["succ_cb"],
+                                        d["anchors"][a:b], w.K))
+    torch.cuda.synchronize(dev)
+    for i, name_i in enumerate(["ids", "unary", "h", "edges"]):
+        got = torch.cat([pt[i] for pt in parts], dim=0)
+        assert torch.equal(got.view(torch.uint8), whole[i].view(torch.uint8)), name_i
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- robustness
 
 def test_topk_fuzz_shapes(dev):
