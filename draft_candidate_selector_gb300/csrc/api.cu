@@ -164,12 +164,13 @@ dflash_status check_ptr(const void* p, const char* name) {
     return DFLASH_OK;
 }
 
-// The anchors are read one id at a time, so their natural 4-byte alignment suffices (a slice
-// of requests out of a larger anchors array stays valid).
-dflash_status check_anchors(const int32_t* p) {
-    if (!p) return fail(DFLASH_INVALID_ARGUMENT, "anchors is NULL");
+// For the arrays that need only their natural 4-byte alignment: the anchors (read one id at
+// a time) and the logits (the top-k finds the 16-byte boundaries itself), so a slice of
+// requests out of larger arrays stays valid.
+dflash_status check_ptr4(const void* p, const char* name) {
+    if (!p) return fail(DFLASH_INVALID_ARGUMENT, "%s is NULL", name);
     if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0)
-        return fail(DFLASH_INVALID_ARGUMENT, "anchors is not 4-byte aligned");
+        return fail(DFLASH_INVALID_ARGUMENT, "%s is not 4-byte aligned", name);
     return DFLASH_OK;
 }
 
@@ -246,7 +247,7 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
     NvtxRange range("dflash_topk_candidates");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
-    DFLASH_TRY(check_ptr(logits, "logits"));
+    DFLASH_TRY(check_ptr4(logits, "logits"));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(workspace, "workspace"));
@@ -267,7 +268,7 @@ dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, 
                                              dflash_stream_t stream) {
     NvtxRange range("dflash_topk_candidates_noalloc");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
-    DFLASH_TRY(check_ptr(logits, "logits"));
+    DFLASH_TRY(check_ptr4(logits, "logits"));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     dflash::DeviceInfo dev;
@@ -352,7 +353,7 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(h, "h"));
-    DFLASH_TRY(check_anchors(anchors));
+    DFLASH_TRY(check_ptr4(anchors, "anchors"));
     DFLASH_TRY(check_ptr(edges, "edges"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
@@ -374,12 +375,12 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
-    DFLASH_TRY(check_ptr(logits, "logits"));
+    DFLASH_TRY(check_ptr4(logits, "logits"));
     DFLASH_TRY(check_ptr(hidden, "hidden"));
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
-    DFLASH_TRY(check_anchors(anchors));
+    DFLASH_TRY(check_ptr4(anchors, "anchors"));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));
@@ -432,7 +433,7 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(hidden, "hidden"));
-    DFLASH_TRY(check_anchors(anchors));
+    DFLASH_TRY(check_ptr4(anchors, "anchors"));
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
@@ -493,7 +494,7 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
-    DFLASH_TRY(check_anchors(anchors));
+    DFLASH_TRY(check_ptr4(anchors, "anchors"));
     DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
     DFLASH_TRY(check_ptr(unary, "unary"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));

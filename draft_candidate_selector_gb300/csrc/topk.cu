@@ -43,7 +43,8 @@ constexpr int kUnroll = 8;              // 128-bit loads per lane per group (4 K
 // 1137 us vs 1184 us, qwen_zipf 118 us vs 111 us.
 constexpr long long kSmallProblemBytes = 2LL << 30;
 constexpr long long kMinSpan = 1024;    // smallest span given to one warp
-constexpr long long kSpanAlign = 128;   // spans start on 512-byte boundaries
+constexpr long long kSpanAlign = 128;   // spans start 512 bytes apart (on 512-byte boundaries
+                                        // when the logits are 16-byte aligned)
 constexpr unsigned kFull = 0xffffffffu;
 
 // Order-preserving map from float bits to uint32: a larger float gives a larger key.
@@ -244,19 +245,21 @@ __device__ __forceinline__ void check_group(WarpList& L, const float4 (&v)[U], u
     }
 }
 
-// Scan flat logits [lo, hi), all inside the row that starts at flat index row_base.
+// Scan flat logits [lo, hi), all inside the row that starts at flat index row_base. `mis` is
+// the base pointer's offset, in floats, from a 16-byte boundary (0 to 3): the 128-bit loads
+// start where the address, not the index, is a multiple of 16 bytes.
 __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict__ logits,
                                            long long lo, long long hi, long long row_base,
-                                           int lane, int K) {
-    // Unaligned head (fewer than 4 logits; only when V is not a multiple of 4).
-    const long long a4 = min(hi, (lo + 3) & ~3LL);
+                                           int lane, int K, int mis) {
+    // Unaligned head (fewer than 4 logits: V not a multiple of 4, or an offset base).
+    const long long a4 = min(hi, ((lo + mis + 3) & ~3LL) - mis);
     if (lo < a4) {
         const long long i = lo + lane;
         const bool valid = i < a4;
         const float v = valid ? logits[i] : 0.f;
         list_offer(L, make_entry(v, (uint32_t)(i - row_base)), valid, lane, K);
     }
-    const long long b4 = max(a4, hi & ~3LL);
+    const long long b4 = max(a4, ((hi + mis) & ~3LL) - mis);
     const float4* __restrict__ p = reinterpret_cast<const float4*>(logits + a4);
     const long long n4 = (b4 - a4) >> 2;
     const uint32_t col0 = (uint32_t)(a4 - row_base);
@@ -300,6 +303,7 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
     if (gw >= warps) return;
     const long long s = gw * span;
     const long long e = min(total, s + span);
+    const int mis = (int)((reinterpret_cast<uintptr_t>(logits) >> 2) & 3);
     const long long r_first = s / V;
     const long long r_last = (e - 1) / V;
 
@@ -309,7 +313,7 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
         const long long hi = min(e, row_base + V);
         WarpList L;
         list_reset(L);
-        scan_range(L, logits, lo, hi, row_base, lane, K);
+        scan_range(L, logits, lo, hi, row_base, lane, K, mis);
 
         // Warps whose spans touch this row.
         const long long w0 = row_base / span;

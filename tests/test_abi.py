@@ -48,6 +48,7 @@ def test_topk_argument_checks(lib):
     assert _topk(lib, K=33) == _native.DFLASH_UNSUPPORTED
     assert _topk(lib, logits=P(None)) == _native.DFLASH_INVALID_ARGUMENT
     assert _topk(lib, ids=MIS) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, logits=P(4098)) == _native.DFLASH_INVALID_ARGUMENT   # 2-byte offset
     assert b"aligned" in lib.dflash_last_error()
     assert _topk(lib, ws=P(None)) == _native.DFLASH_INVALID_ARGUMENT
     assert _topk(lib, cap=-1.0) == _native.DFLASH_INVALID_ARGUMENT

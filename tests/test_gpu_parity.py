@@ -687,15 +687,47 @@ def test_selector_request_chunks_equal_one_call(dev, name):
     for a, b in zip(cuts[:-1], cuts[1:]):
         if a == b:
             continue
-        # Copies of the logits and hidden slices (16-byte aligned, as the header asks; with
-        # V % 4 != 0 a slice of the logits is not). The anchors slice is a plain view.
-        parts.append(ds.dflash_selector(d["logits"][a:b].clone(), d["hidden"][a:b].clone(),
-                                        d["w_proj"], d["pred_cb"], d["succ_cb"],
-                                        d["anchors"][a:b], w.K))
+        # Views: the logits and anchors need only 4-byte alignment; hidden (H % 8 == 0) stays
+        # 16-byte aligned under any request slice.
+        parts.append(ds.dflash_selector(d["logits"][a:b], d["hidden"][a:b], d["w_proj"],
+                                        d["pred_cb"], d["succ_cb"], d["anchors"][a:b], w.K))
     torch.cuda.synchronize(dev)
     for i, name_i in enumerate(["ids", "unary", "h", "edges"]):
         got = torch.cat([pt[i] for pt in parts], dim=0)
         assert torch.equal(got.view(torch.uint8), whole[i].view(torch.uint8)), name_i
+    _status_clean()
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_topk_logits_off_16_byte_boundary(dev, offset):
+    """Logits that start 4, 8 or 12 bytes past a 16-byte boundary (a slice of requests out of
+    a larger array): the top-k must find the boundaries itself and give the oracle's result,
+    alone and inside the fused selector."""
+    rng = np.random.default_rng(40 + offset)
+    for (R, S, V, K) in [(3, 5, 1001, 8), (2, 3, 70003, 32), (4, 2, 17, 5)]:
+        x = (rng.standard_normal((R, S, V)) * 3).astype(np.float32)
+        x[0, 0, ::7] = 2.0                                    # ties
+        base = torch.empty(R * S * V + 8, dtype=torch.float32, device=dev)
+        view = base[offset:offset + R * S * V].view(R, S, V)
+        view.copy_(torch.from_numpy(x))
+        assert view.data_ptr() % 16 == 4 * offset
+        ids, un = ds.dflash_topk_candidates(view, K)
+        ref_ids, ref_un = oracle.topk(x, K)
+        P.assert_ids_equal(ids.cpu().numpy(), ref_ids, f"offset {offset} R={R} V={V}")
+        P.assert_close(un.cpu().numpy(), ref_un, f"offset {offset} R={R} V={V}")
+    inp = host_inputs("small_ties")
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    base = torch.empty(d["logits"].numel() + 8, dtype=torch.float32, device=dev)
+    view = base[offset:offset + d["logits"].numel()].view(d["logits"].shape)
+    view.copy_(d["logits"])
+    got = ds.dflash_selector(view, d["hidden"], d["w_proj"], d["pred_cb"], d["succ_cb"],
+                             d["anchors"], w.K)
+    want = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"], d["succ_cb"],
+                              d["anchors"], w.K)
+    torch.cuda.synchronize(dev)
+    for a, b in zip(got, want):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     _status_clean()
 
 
