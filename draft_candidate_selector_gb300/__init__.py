@@ -30,7 +30,7 @@ __all__ = [
     "dflash_selector_workspace_bytes", "dflash_lmhead_topk_workspace_bytes",
     "dflash_selector_lmhead_workspace_bytes",
     "dflash_device_status", "dflash_trace_begin", "dflash_trace_end", "DflashError",
-    "library_path",
+    "library_path", "CandidateSelector",
 ]
 
 
@@ -361,3 +361,6 @@ def dflash_trace_end(max_calls: int) -> list[tuple[float, float, float]]:
     n = ctypes.c_int(0)
     _native.check(_native.load().dflash_trace_end(buf, int(max_calls), ctypes.byref(n)))
     return [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n.value)]
+
+
+from .selector import CandidateSelector  # noqa: E402  (uses the functions above)

@@ -194,3 +194,15 @@ def test_anchors_need_only_natural_alignment(lib):
         assert st == expect_ok
     assert f(A, A, A, A, A, bad2, 2, 3, 4, 100, 16, A, None) == _native.DFLASH_INVALID_ARGUMENT
     assert b"anchors" in lib.dflash_last_error()
+
+
+def test_candidate_selector_module_host_checks():
+    """The module-style holder keeps the page's names and refuses non-bf16 weights."""
+    import draft_candidate_selector_gb300 as ds
+    sel = ds.CandidateSelector(64, 100, 16, 4, device="cpu")
+    assert sel.predecessor_codebook.shape == (100, 16)
+    assert sel.successor_codebook.shape == (100, 16)
+    assert sel.hidden_projection_weight.shape == (16, 64)
+    assert sel.predecessor_codebook.dtype == torch.bfloat16
+    with pytest.raises(NotImplementedError):
+        ds.CandidateSelector(64, 100, 16, 4, device="cpu", params_dtype=torch.float16)

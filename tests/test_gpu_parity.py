@@ -731,6 +731,30 @@ def test_topk_logits_off_16_byte_boundary(dev, offset):
     _status_clean()
 
 
+def test_candidate_selector_module(dev):
+    """The module-style holder runs the same calls: forward equals dflash_selector_forward,
+    select equals dflash_selector, both bit for bit."""
+    inp = host_inputs("small_ties")
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    sel = ds.CandidateSelector(w.H, w.V, w.rank, w.K, device=dev)
+    sel.predecessor_codebook.copy_(d["pred_cb"])
+    sel.successor_codebook.copy_(d["succ_cb"])
+    sel.hidden_projection_weight.copy_(d["w_proj"])
+    ids, un, edges = sel.select(d["logits"], d["hidden"], d["anchors"])
+    r_ids, r_un, _, r_e = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                                             d["succ_cb"], d["anchors"], w.K)
+    e2 = sel(ids, un, d["hidden"], d["anchors"])
+    torch.cuda.synchronize(dev)
+    assert torch.equal(ids, r_ids) and torch.equal(un.view(torch.int32), r_un.view(torch.int32))
+    assert torch.equal(edges.view(torch.int32), r_e.view(torch.int32))
+    assert torch.equal(e2.view(torch.int32), r_e.view(torch.int32))
+    path, tokens, _ = sel.best_path(edges, ids)
+    ref_path, ref_tokens, _ = oracle.best_path(edges.cpu().numpy(), ids.cpu().numpy())
+    P.assert_ids_equal(tokens.cpu().numpy(), ref_tokens, "module best path tokens")
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- robustness
 
 def test_topk_fuzz_shapes(dev):
