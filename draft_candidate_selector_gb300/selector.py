@@ -12,7 +12,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (dflash_best_path, dflash_selector, dflash_selector_forward,
+from . import (dflash_best_path, dflash_lmhead_topk, dflash_selector, dflash_selector_forward,
                dflash_selector_lmhead)
 
 
@@ -59,6 +59,14 @@ class CandidateSelector:
             logits, hidden_states, self.hidden_projection_weight, self.predecessor_codebook,
             self.successor_codebook, anchor_token_ids, self.top_k, softcap=softcap, scale=scale)
         return ids, unary, edges
+
+    def compute_candidates(self, hidden_states: torch.Tensor, lm_head: torch.Tensor,
+                           softcap: float = 0.0, scale: float = 1.0):
+        """The top_k candidate ids and their (processed) logits at each position, straight
+        from the LM head [V, H] without logits in memory, as the page's
+        DFlash2BeamForCausalLM.compute_candidates gives them (dflash_lmhead_topk)."""
+        return dflash_lmhead_topk(hidden_states, lm_head, self.top_k, softcap=softcap,
+                                  scale=scale)
 
     def select_from_lm_head(self, hidden_states: torch.Tensor, lm_head: torch.Tensor,
                             anchor_token_ids: torch.Tensor, softcap: float = 0.0,

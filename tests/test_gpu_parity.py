@@ -752,6 +752,12 @@ def test_candidate_selector_module(dev):
     path, tokens, _ = sel.best_path(edges, ids)
     ref_path, ref_tokens, _ = oracle.best_path(edges.cpu().numpy(), ids.cpu().numpy())
     P.assert_ids_equal(tokens.cpu().numpy(), ref_tokens, "module best path tokens")
+    lm = (torch.randn((w.V, w.H), device=dev) / w.H ** 0.5).to(torch.bfloat16)
+    c_ids, c_un = sel.compute_candidates(d["hidden"], lm)
+    l_ids, l_un, l_e = sel.select_from_lm_head(d["hidden"], lm, d["anchors"])
+    torch.cuda.synchronize(dev)
+    assert torch.equal(c_ids, l_ids) and torch.equal(c_un.view(torch.int32), l_un.view(torch.int32))
+    assert l_e.shape == (w.R, w.S, w.K, w.K)
     _status_clean()
 
 
