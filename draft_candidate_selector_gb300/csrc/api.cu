@@ -164,9 +164,10 @@ dflash_status check_ptr(const void* p, const char* name) {
     return DFLASH_OK;
 }
 
-// For the arrays that need only their natural 4-byte alignment: the anchors (read one id at
-// a time) and the logits (the top-k finds the 16-byte boundaries itself), so a slice of
-// requests out of larger arrays stays valid.
+// For the arrays that need only their natural 4-byte alignment: the anchors, candidate ids,
+// unary values, edge scores and best-path outputs (read and written one element at a time,
+// or staged with copies as wide as their alignment allows) and the logits (the top-k finds
+// the 16-byte boundaries itself), so a slice of requests out of larger arrays stays valid.
 dflash_status check_ptr4(const void* p, const char* name) {
     if (!p) return fail(DFLASH_INVALID_ARGUMENT, "%s is NULL", name);
     if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0)
@@ -248,8 +249,8 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_processor(softcap, scale));
     DFLASH_TRY(check_ptr4(logits, "logits"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     DFLASH_TRY(check_ptr(workspace, "workspace"));
     dflash::DeviceInfo dev;
     DFLASH_TRY(current_device(&dev, nullptr));
@@ -269,8 +270,8 @@ dflash_status dflash_topk_candidates_noalloc(const float* logits, int R, int S, 
     NvtxRange range("dflash_topk_candidates_noalloc");
     DFLASH_TRY(check_dims_topk(R, S, V, K));
     DFLASH_TRY(check_ptr4(logits, "logits"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     dflash::DeviceInfo dev;
     DFLASH_TRY(current_device(&dev, nullptr));
     const dflash::TopkPlan plan = dflash::topk_plan(dev, (long long)R * S, V);
@@ -307,8 +308,8 @@ dflash_status dflash_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head
     if (H % 8 != 0) return fail(DFLASH_UNSUPPORTED, "H=%d: must be a multiple of 8", H);
     DFLASH_TRY(check_ptr(hidden, "hidden"));
     DFLASH_TRY(check_ptr(lm_head, "lm_head"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     DFLASH_TRY(check_ptr(workspace, "workspace"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
@@ -350,11 +351,11 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
     DFLASH_TRY(check_dims_edges(R, S, K, V, rank));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     DFLASH_TRY(check_ptr(h, "h"));
     DFLASH_TRY(check_ptr4(anchors, "anchors"));
-    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr4(edges, "edges"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
     DFLASH_TRY(current_device(&dev, &status));
@@ -381,10 +382,10 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
     DFLASH_TRY(check_ptr4(anchors, "anchors"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));
-    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr4(edges, "edges"));
     DFLASH_TRY(check_ptr(workspace, "workspace"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
@@ -430,15 +431,15 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
     NvtxRange range("dflash_selector_forward");
     DFLASH_TRY(check_dims_edges(R, S, K, V, rank));
     DFLASH_TRY(check_dims_projection(R, S, H, rank));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     DFLASH_TRY(check_ptr(hidden, "hidden"));
     DFLASH_TRY(check_ptr4(anchors, "anchors"));
     DFLASH_TRY(check_ptr(w_proj, "w_proj"));
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));
-    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr4(edges, "edges"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
     DFLASH_TRY(current_device(&dev, &status));
@@ -462,11 +463,11 @@ dflash_status dflash_best_path(const float* edges, const int32_t* cand_ids, int 
     if (S > dflash::kMaxPathSteps)
         return fail(DFLASH_UNSUPPORTED, "S=%d: the best path supports S <= %d", S,
                     dflash::kMaxPathSteps);
-    DFLASH_TRY(check_ptr(edges, "edges"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(path, "path"));
-    DFLASH_TRY(check_ptr(tokens, "tokens"));
-    DFLASH_TRY(check_ptr(score, "score"));
+    DFLASH_TRY(check_ptr4(edges, "edges"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(path, "path"));
+    DFLASH_TRY(check_ptr4(tokens, "tokens"));
+    DFLASH_TRY(check_ptr4(score, "score"));
     DFLASH_TRY(current_device(nullptr, nullptr));
     cudaError_t e = dflash::launch_best_path(edges, cand_ids, R, S, K, path, tokens, score,
                                              reinterpret_cast<cudaStream_t>(stream));
@@ -495,10 +496,10 @@ dflash_status dflash_selector_lmhead(const uint16_t* hidden, const uint16_t* lm_
     DFLASH_TRY(check_ptr(pred_cb, "pred_cb"));
     DFLASH_TRY(check_ptr(succ_cb, "succ_cb"));
     DFLASH_TRY(check_ptr4(anchors, "anchors"));
-    DFLASH_TRY(check_ptr(cand_ids, "cand_ids"));
-    DFLASH_TRY(check_ptr(unary, "unary"));
+    DFLASH_TRY(check_ptr4(cand_ids, "cand_ids"));
+    DFLASH_TRY(check_ptr4(unary, "unary"));
     DFLASH_TRY(check_ptr(h_out, "h_out"));
-    DFLASH_TRY(check_ptr(edges, "edges"));
+    DFLASH_TRY(check_ptr4(edges, "edges"));
     DFLASH_TRY(check_ptr(workspace, "workspace"));
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;

@@ -18,7 +18,7 @@
 // E[r,p,q,c], reduces them with a 3-level tree, and two ordered shuffle levels combine the
 // four quarters; every combine keeps exactly the running maximum's choice (scan_combine). The
 // CTA stages the K x K blocks of the next steps in a shared-memory ring with cp.async
-// (16-byte copies when K is even, 4-byte ones otherwise), so a step's update runs while
+// (16-byte copies when K is even and the scores are 16-byte aligned, 4-byte ones otherwise), so a step's update runs while
 // later steps' blocks are in flight; one barrier per step. V_{p-1} is double-buffered in
 // shared memory, and the kept predecessors go to shared memory (S x 32 bytes). Thread 0
 // takes the last step's choice and walks the kept predecessors back; the threads then write
@@ -62,14 +62,15 @@ __device__ __forceinline__ void cp_async_wait_ring() {
     asm volatile("cp.async.wait_group %0;" ::"n"(kDepth - 2) : "memory");
 }
 
-// This thread's share of the copy of step p's K x K block into ring stage p % kDepth. With K
-// even, every block starts on a 16-byte boundary (the edge scores are 16-byte aligned), so
-// the copy moves 16 bytes per thread and instruction; with K odd, 4.
-__device__ __forceinline__ void stage_step(float* ring, const float* E, int p, int K, int tid) {
+// This thread's share of the copy of step p's K x K block into ring stage p % kDepth. When
+// every block starts on a 16-byte boundary (K even and a 16-byte aligned base; `wide`), the
+// copy moves 16 bytes per thread and instruction; otherwise 4.
+__device__ __forceinline__ void stage_step(float* ring, const float* E, int p, int K, int tid,
+                                           bool wide) {
     const int n = K * K;
     float* dst = ring + (size_t)(p % kDepth) * n;
     const float* src = E + (size_t)p * n;
-    if ((K & 1) == 0) {
+    if (wide) {
         for (int i = tid * 4; i < n; i += kThreads * 4) cp_async16(dst + i, src + i);
     } else {
         for (int i = tid; i < n; i += kThreads) cp_async4(dst + i, src + i);
@@ -122,9 +123,10 @@ best_path_kernel(const float* __restrict__ edges, const int32_t* __restrict__ ca
     uint8_t* chosen = keep + (size_t)S * 32;                             // [S]
     const float* E = edges + (size_t)r * S * K * K;
     const bool live = c < K;
+    const bool wide = (K & 1) == 0 && (reinterpret_cast<uintptr_t>(edges) & 15) == 0;
 
     for (int p = 0; p < kDepth; ++p) {                   // prologue: steps 0 .. kDepth-1
-        if (p < S) stage_step(ring, E, p, K, tid);
+        if (p < S) stage_step(ring, E, p, K, tid, wide);
         cp_async_commit();
     }
     for (int p = 0; p < S; ++p) {
@@ -134,7 +136,7 @@ best_path_kernel(const float* __restrict__ edges, const int32_t* __restrict__ ca
             // Refill the stage step p-1 used. One group per step, empty past the last step,
             // so that before step p's wait exactly p + kDepth - 1 groups are committed and
             // waiting for all but the newest kDepth - 2 covers step p.
-            if (p - 1 + kDepth < S) stage_step(ring, E, p - 1 + kDepth, K, tid);
+            if (p - 1 + kDepth < S) stage_step(ring, E, p - 1 + kDepth, K, tid, wide);
             cp_async_commit();
         }
         const float* Ep = ring + (size_t)(p % kDepth) * K * K;

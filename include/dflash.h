@@ -21,9 +21,12 @@
  *     comment says otherwise. Tensors are contiguous and row-major, in the shapes given.
  *     bf16 tensors are passed as uint16_t bit patterns.
  *   - Every pointer must be 16-byte aligned (vector loads and TMA), or the call returns
- *     DFLASH_INVALID_ARGUMENT. The exceptions are `anchors` (read one id at a time) and
- *     `logits` (the top-k finds the 16-byte boundaries itself): their natural 4-byte
- *     alignment suffices, so a slice of requests out of larger arrays stays valid.
+ *     DFLASH_INVALID_ARGUMENT. The exceptions are `logits` (the top-k finds the 16-byte
+ *     boundaries itself), `anchors`, `cand_ids`, `unary`, `edges` and the best path's
+ *     `path`, `tokens` and `score` (accessed one element at a time, or staged with copies
+ *     as wide as their alignment allows): their natural
+ *     4-byte alignment suffices, so a slice of requests out of larger arrays stays valid.
+ *     `hidden`, `h_out`, the weights and the workspace stay 16-byte aligned.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream). They
  *     allocate no device memory and do not synchronise the device; dflash_device_status,
  *     dflash_trace_end and dflash_selftest_wait_timeout are the exceptions, and say so. A

@@ -47,7 +47,7 @@ def test_topk_argument_checks(lib):
     assert _topk(lib, K=101, V=100) == _native.DFLASH_INVALID_ARGUMENT
     assert _topk(lib, K=33) == _native.DFLASH_UNSUPPORTED
     assert _topk(lib, logits=P(None)) == _native.DFLASH_INVALID_ARGUMENT
-    assert _topk(lib, ids=MIS) == _native.DFLASH_INVALID_ARGUMENT
+    assert _topk(lib, ids=P(4098)) == _native.DFLASH_INVALID_ARGUMENT     # 2-byte offset
     assert _topk(lib, logits=P(4098)) == _native.DFLASH_INVALID_ARGUMENT   # 2-byte offset
     assert b"aligned" in lib.dflash_last_error()
     assert _topk(lib, ws=P(None)) == _native.DFLASH_INVALID_ARGUMENT
@@ -177,7 +177,7 @@ def test_best_path_argument_checks(lib):
     assert f(A, A, 2, 3, 0, A, A, A, None) == _native.DFLASH_INVALID_ARGUMENT
     assert f(A, A, 2, 3, 33, A, A, A, None) == _native.DFLASH_UNSUPPORTED
     assert f(A, A, 2, 257, 4, A, A, A, None) == _native.DFLASH_UNSUPPORTED
-    assert f(MIS, A, 2, 3, 4, A, A, A, None) == _native.DFLASH_INVALID_ARGUMENT
+    assert f(P(4098), A, 2, 3, 4, A, A, A, None) == _native.DFLASH_INVALID_ARGUMENT  # 2-byte
     assert f(A, A, 2, 3, 4, A, P(None), A, None) == _native.DFLASH_INVALID_ARGUMENT
     if not torch.cuda.is_available():
         assert f(A, A, 2, 3, 4, A, A, A, None) == _native.DFLASH_NO_DEVICE

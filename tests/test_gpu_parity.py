@@ -493,6 +493,51 @@ def test_best_path_ties_and_edge_shapes(dev):
     _status_clean()
 
 
+def test_odd_k_request_slices(dev):
+    """With K odd, request slices of the candidate ids, unary values, edge scores and the
+    best path's outputs start off 16-byte boundaries. Those arrays need only 4-byte alignment:
+    the fused selector writing into slices, the forward pass reading them and the best path
+    staging them equal calls on whole, aligned arrays."""
+    w = wl.custom_workload(5, 3, 7, 3001, 64, 16)
+    d = P.to_device(wl.make_inputs(w, seed=0), dev)
+    ids, un, h, e = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
+                                       d["succ_cb"], d["anchors"], w.K)
+    a, b = 1, 4                                   # requests 1..3
+    s_ids, s_un, s_h, s_e = (torch.empty_like(x) for x in (ids, un, h, e))
+    ds.dflash_selector(d["logits"][a:b], d["hidden"][a:b], d["w_proj"], d["pred_cb"],
+                       d["succ_cb"], d["anchors"][a:b], w.K, s_ids[a:b], s_un[a:b], s_h[a:b],
+                       s_e[a:b])
+    assert s_ids[a:b].data_ptr() % 16 != 0 and s_e[a:b].data_ptr() % 16 != 0
+    assert d["logits"][a:b].data_ptr() % 16 != 0
+    assert torch.equal(s_ids[a:b], ids[a:b])
+    assert torch.equal(s_un[a:b].view(torch.int32), un[a:b].view(torch.int32))
+    assert torch.equal(s_e[a:b].view(torch.int32), e[a:b].view(torch.int32))
+    _, f_e = ds.dflash_selector_forward(ids[a:b], un[a:b], d["hidden"][a:b], d["anchors"][a:b],
+                                        d["w_proj"], d["pred_cb"], d["succ_cb"])
+    assert torch.equal(f_e.view(torch.int32), e[a:b].view(torch.int32))
+    path = torch.zeros((w.R, w.S), dtype=torch.int32, device=dev)
+    tokens = torch.zeros_like(path)
+    score = torch.zeros((w.R,), dtype=torch.float32, device=dev)
+    ds.dflash_best_path(e[a:b], ids[a:b], path[a:b], tokens[a:b], score[a:b])
+    rp, rt, rs = oracle.best_path(e[a:b].cpu().numpy(), ids[a:b].cpu().numpy())
+    P.assert_ids_equal(path[a:b].cpu().numpy(), rp, "best path on a slice")
+    P.assert_ids_equal(tokens[a:b].cpu().numpy(), rt, "best path tokens on a slice")
+    assert np.array_equal(score[a:b].cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    # K even with the edge scores off a 16-byte boundary: the path stages with 4-byte copies
+    rng = np.random.default_rng(9)
+    flat = rng.standard_normal(4 * 5 * 8 * 8 + 2).astype(np.float32)
+    big = torch.from_numpy(flat).to(dev)
+    e8 = big[2:].view(4, 5, 8, 8)
+    c8 = torch.from_numpy(rng.integers(0, 100, (4, 5, 8)).astype(np.int32)).to(dev)
+    assert e8.data_ptr() % 16 == 8
+    p8, t8, s8 = ds.dflash_best_path(e8, c8)
+    rp8, rt8, rs8 = oracle.best_path(e8.cpu().numpy(), c8.cpu().numpy())
+    P.assert_ids_equal(p8.cpu().numpy(), rp8, "best path, offset base")
+    P.assert_ids_equal(t8.cpu().numpy(), rt8, "best path tokens, offset base")
+    assert np.array_equal(s8.cpu().numpy().view(np.uint32), rs8.view(np.uint32))
+    _status_clean()
+
+
 # ----------------------------------------------------------------------------- candidate head from the LM head
 
 def _bf16(t):
