@@ -372,6 +372,23 @@ def run_ours(args, w: wl.Workload) -> None:
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1) / args.e2e_steps, w.edges_per_call, world)
 
+    # The host link's own rate, the bound of the e2e number: the same chunked host-to-device
+    # copies as one e2e step, alone on the copy stream with nothing else running, best of two.
+    link_ms = []
+    for _ in range(2):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(copy_in)
+        with torch.cuda.stream(copy_in):
+            for c in range(nch):
+                r0, r1 = bounds[c], bounds[c + 1]
+                logits[r0:r1].copy_(logits_host[r0:r1], non_blocking=True)
+                hidden[r0:r1].copy_(hidden_host[r0:r1], non_blocking=True)
+                anchors[r0:r1].copy_(anchors_host[r0:r1], non_blocking=True)
+        l1.record(copy_in)
+        torch.cuda.synchronize(dev)
+        link_ms.append(l0.elapsed_time(l1))
+    link_gbs = h2d / (min(link_ms) / 1e3) / 1e9
+
     if rank == 0:
         topk_ms = statistics.mean(s[1] for s in stages)
         proj_ms = statistics.mean(s[0] for s in stages)
@@ -405,7 +422,9 @@ def run_ours(args, w: wl.Workload) -> None:
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipeline_chunks": nch,
-                    "h2d_gbs_effective": h2d / (e2e_ms / 1e3) / 1e9},
+                    "h2d_gbs_effective": h2d / (e2e_ms / 1e3) / 1e9,
+                    "link_h2d_gbs_measured": link_gbs,
+                    "link_frac": h2d / (e2e_ms / 1e3) / 1e9 / link_gbs},
             "gpu_launches": 3 * args.steps,   # projection, top-k, edges per step
             "device_status": status,
             "clocks": clocks.summary(),

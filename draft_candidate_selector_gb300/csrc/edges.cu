@@ -26,8 +26,6 @@
 // kStatusBadId. No thread waits on another CTA.
 #include "common.cuh"
 
-#include <cuda_bf16.h>
-
 #include <mutex>
 
 namespace dflash {
@@ -71,22 +69,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// (x, y) -> packed bf16 pair (x in the low half), round to nearest even.
-__device__ __forceinline__ uint32_t pack2(float x, float y) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(x, y);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Two exact products pred*h from one 32-bit word of each, split into a packed hi pair
-// and a packed lo pair (see the file comment).
+// Two products pred*h from one 32-bit word (two bf16) of each, split into a packed hi pair
+// and a packed lo pair with hi + lo = pred*h exactly (see the file comment). Each half is
+// one bf16x2 fused multiply-add, which rounds the exact product once: hi = RN(a*b) (the
+// addend is -0), lo = RN(a*b - hi). The product of two 8-bit significands has at most 16
+// bits and its rounding remainder at most 8, so lo is exact.
 __device__ __forceinline__ void split_pair(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
-    const float x = bf16_lo(a) * bf16_lo(b);
-    const float y = bf16_hi(a) * bf16_hi(b);
-    hi = pack2(x, y);
-    lo = pack2(x - bf16_lo(hi), y - bf16_hi(hi));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(a), "r"(b), "r"(0x80008000u));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(a), "r"(b), "r"(hi ^ 0x80008000u));
 }
 
 struct EdgeSmem {

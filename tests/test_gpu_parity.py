@@ -287,6 +287,36 @@ def test_edges_bad_ids_are_reported_not_followed(dev):
     P.assert_close(e.cpu().numpy(), ref, "edges with bad ids")
 
 
+@pytest.mark.parametrize("R,S,K,V,rank", [
+    (400, 15, 23, 5000, 40),      # padded contraction (40 -> 48), ragged K
+    (160, 15, 32, 262144, 256),   # the largest layout
+])
+def test_edges_many_waves_with_bad_ids(dev, R, S, K, V, rank):
+    """Thousands of (r, p) tiles, several waves of CTAs per SM, with bad ids sprinkled in:
+    every score equals the oracle's, bad rows and columns are NaN, and the status bit is
+    set."""
+    rng = np.random.default_rng(R + K + rank)
+    g = torch.Generator().manual_seed(R + rank)
+    pred = (torch.randn(V, rank, generator=g) / rank ** 0.5).to(torch.bfloat16)
+    succ = (torch.randn(V, rank, generator=g) / rank ** 0.5).to(torch.bfloat16)
+    ids = rng.integers(0, V, (R, S, K)).astype(np.int32)
+    bad = rng.choice(R * S * K, 7, replace=False)
+    ids.reshape(-1)[bad[:4]] = V + rng.integers(0, 100, 4)
+    ids.reshape(-1)[bad[4:]] = -1 - rng.integers(0, 100, 3)
+    un = rng.standard_normal((R, S, K)).astype(np.float32)
+    h = P.bits(torch.randn(R, S, rank, generator=g).to(torch.bfloat16))
+    anchors = rng.integers(0, V, R).astype(np.int32)
+    anchors[R // 2] = V                            # one bad anchor
+    ds.dflash_device_status(clear=True)
+    e = ds.dflash_candidate_edges(
+        pred.to(dev), succ.to(dev), torch.from_numpy(ids).to(dev), torch.from_numpy(un).to(dev),
+        torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev),
+        torch.from_numpy(anchors).to(dev))
+    assert ds.dflash_device_status(clear=True) & ds.DEVICE_BAD_ID
+    ref = oracle.edges(P.bits(pred), P.bits(succ), ids, un, h, anchors, allow_bad_ids=True)
+    P.assert_close(e.cpu().numpy(), ref, f"edges, many waves, K={K} rank={rank}")
+
+
 # ----------------------------------------------------------------------------- fused selector
 
 def _selector_check(dev, inp: wl.Inputs, req: np.ndarray | None, what: str):
