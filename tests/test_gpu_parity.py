@@ -265,6 +265,31 @@ def test_edges_shapes(dev, R, S, K, V, rank):
     _status_clean()
 
 
+def test_edges_subnormal_codebook_entries(dev):
+    """Products are taken as in fp32, subnormal bf16 inputs included: pred entries of 2^-130
+    (subnormal), h = 2^100 and succ = 2^20 give 2^-10 per term and exactly 16 * 2^-10 = 2^-6
+    per score over rank 16. Flushing the subnormal inputs would give 0."""
+    R, S, K, V, rank = 1, 2, 2, 4, 16
+    sub, big_h, big_s = np.uint16(0x0008), np.uint16(0x7180), np.uint16(0x4980)
+    assert float(oracle.bits_to_float(np.array([sub]))[0]) == 2.0 ** -130
+    assert float(oracle.bits_to_float(np.array([big_h]))[0]) == 2.0 ** 100
+    assert float(oracle.bits_to_float(np.array([big_s]))[0]) == 2.0 ** 20
+    pred = np.full((V, rank), sub, dtype=np.uint16)
+    succ = np.full((V, rank), big_s, dtype=np.uint16)
+    ids = np.array([[[0, 1], [2, 3]]], dtype=np.int32)
+    un = np.zeros((R, S, K), dtype=np.float32)
+    h = np.full((R, S, rank), big_h, dtype=np.uint16)
+    anchors = np.array([3], dtype=np.int32)
+    as_bf16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    e = ds.dflash_candidate_edges(as_bf16(pred), as_bf16(succ), torch.from_numpy(ids).to(dev),
+                                  torch.from_numpy(un).to(dev), as_bf16(h),
+                                  torch.from_numpy(anchors).to(dev))
+    ref = oracle.edges(pred, succ, ids, un, h, anchors)
+    assert np.all(ref == 2.0 ** -6)
+    assert np.array_equal(e.cpu().numpy(), ref.astype(np.float32))
+    _status_clean()
+
+
 def test_edges_bad_ids_are_reported_not_followed(dev):
     """An anchor or candidate id outside [0, V) gives NaN scores and sets the status bit."""
     R, S, K, V, rank = 2, 3, 4, 50, 16
