@@ -227,10 +227,10 @@ __device__ __forceinline__ void first_group(WarpList& L, const float4* __restric
     }
 }
 
-// Check one group of U float4 per lane (flat float4 index j + u*32 + lane) against the list.
+// Check one group of U float4 per lane (row float4 index j + u*32 + lane) against the list.
 template <int U>
 __device__ __forceinline__ void check_group(WarpList& L, const float4 (&v)[U], uint32_t col0,
-                                            long long j, int lane, int K) {
+                                            int j, int lane, int K) {
     bool hit = false;
 #pragma unroll
     for (int u = 0; u < U; ++u) hit |= may_enter(v[u], L.thr_f);
@@ -245,39 +245,40 @@ __device__ __forceinline__ void check_group(WarpList& L, const float4 (&v)[U], u
     }
 }
 
-// Scan flat logits [lo, hi), all inside the row that starts at flat index row_base. `mis` is
-// the base pointer's offset, in floats, from a 16-byte boundary (0 to 3): the 128-bit loads
-// start where the address, not the index, is a multiple of 16 bytes.
-__device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict__ logits,
-                                           long long lo, long long hi, long long row_base,
-                                           int lane, int K, int mis) {
+// Scan logits [lo, hi) of one row, given as indices within the row (0 <= lo < hi <= V), with
+// `row` pointing at the row's first logit. `mis` is that pointer's offset, in floats, from a
+// 16-byte boundary (0 to 3): the 128-bit loads start where the address, not the index, is a
+// multiple of 16 bytes. All indices fit 32 bits because V does.
+template <int U>
+__device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict__ row, int lo,
+                                           int hi, int lane, int K, int mis) {
     // Unaligned head (fewer than 4 logits: V not a multiple of 4, or an offset base).
-    const long long a4 = min(hi, ((lo + mis + 3) & ~3LL) - mis);
+    const int a4 = (int)min((long long)hi, (((long long)lo + mis + 3) & ~3LL) - mis);
     if (lo < a4) {
-        const long long i = lo + lane;
+        const int i = lo + lane;
         const bool valid = i < a4;
-        const float v = valid ? logits[i] : 0.f;
-        list_offer(L, make_entry(v, (uint32_t)(i - row_base)), valid, lane, K);
+        const float v = valid ? row[i] : 0.f;
+        list_offer(L, make_entry(v, (uint32_t)i), valid, lane, K);
     }
-    const long long b4 = max(a4, ((hi + mis) & ~3LL) - mis);
-    const float4* __restrict__ p = reinterpret_cast<const float4*>(logits + a4);
-    const long long n4 = (b4 - a4) >> 2;
-    const uint32_t col0 = (uint32_t)(a4 - row_base);
+    const int b4 = (int)max((long long)a4, (((long long)hi + mis) & ~3LL) - mis);
+    const float4* __restrict__ p = reinterpret_cast<const float4*>(row + a4);
+    const int n4 = (b4 - a4) >> 2;
+    const uint32_t col0 = (uint32_t)a4;
 
-    constexpr long long kGroup = 32LL * kUnroll;     // float4s per group: 32 lines of 128 B
-    long long j = 0;
+    constexpr int kGroup = 32 * U;                   // float4s per group: U lines of 512 B
+    int j = 0;
     if (kGroup <= n4 && L.thr == 0) {                // a full first group, list still empty
-        first_group<kUnroll>(L, p, col0, lane, K);
+        first_group<U>(L, p, col0, lane, K);
         j = kGroup;
     }
     for (; j + kGroup <= n4; j += kGroup) {
-        float4 v[kUnroll];
+        float4 v[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream(p + j + u * 32 + lane);
-        check_group<kUnroll>(L, v, col0, j, lane, K);
+        for (int u = 0; u < U; ++u) v[u] = ld_stream(p + j + u * 32 + lane);
+        check_group<U>(L, v, col0, j, lane, K);
     }
     for (; j < n4; j += 32) {
-        const long long idx = j + lane;
+        const int idx = j + lane;
         const bool valid = idx < n4;
         const float4 v = valid ? ld_stream(p + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
         if (__any_sync(kFull, valid && may_enter(v, L.thr_f)))
@@ -285,46 +286,51 @@ __device__ __forceinline__ void scan_range(WarpList& L, const float* __restrict_
     }
     // Unaligned tail (fewer than 4 logits).
     if (b4 < hi) {
-        const long long i = b4 + lane;
+        const int i = b4 + lane;
         const bool valid = i < hi;
-        const float v = valid ? logits[i] : 0.f;
-        list_offer(L, make_entry(v, (uint32_t)(i - row_base)), valid, lane, K);
+        const float v = valid ? row[i] : 0.f;
+        list_offer(L, make_entry(v, (uint32_t)i), valid, lane, K);
     }
 }
 
-template <int kMinBlocks>
+template <int kMinBlocks, int U>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 topk_kernel(const float* __restrict__ logits, long long total, long long span, int warps, int V,
             int K, float softcap, float scale, int32_t* __restrict__ cand_ids,
             float* __restrict__ unary, uint32_t* __restrict__ counters,
             uint64_t* __restrict__ partials) {
     const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (gw >= warps) return;
-    const long long s = gw * span;
-    const long long e = min(total, s + span);
+    // The warp's span [gw * span, min(total, (gw + 1) * span)) is recomputed where it is
+    // needed rather than kept live across the scan, which holds the register budget.
     const int mis = (int)((reinterpret_cast<uintptr_t>(logits) >> 2) & 3);
-    const long long r_first = s / V;
-    const long long r_last = (e - 1) / V;
+    const int r_first = (int)(((long long)gw * span) / V);
+    const int r_last = (int)((min(total, (long long)gw * span + span) - 1) / V);
 
-    for (long long r = r_first; r <= r_last; ++r) {
-        const long long row_base = r * V;
-        const long long lo = max(s, row_base);
-        const long long hi = min(e, row_base + V);
+    for (int r = r_first; r <= r_last; ++r) {
+        const long long row_base = (long long)r * V;
+        int lo, hi;                              // this warp's part of row r, within the row
+        {
+            const long long s = (long long)gw * span;
+            const long long e = min(total, s + span);
+            lo = (int)(max(s, row_base) - row_base);
+            hi = (int)(min(e, row_base + V) - row_base);
+        }
         WarpList L;
         list_reset(L);
-        scan_range(L, logits, lo, hi, row_base, lane, K, mis);
+        scan_range<U>(L, logits + row_base, lo, hi, lane, K, (int)((mis + row_base) & 3));
 
         // Warps whose spans touch this row.
-        const long long w0 = row_base / span;
-        const long long w1 = (row_base + V - 1) / span;
+        const int w0 = (int)(row_base / span);
+        const int w1 = (int)((row_base + V - 1) / span);
         if (w0 == w1) {
             write_row(L.e, r, lane, K, softcap, scale, cand_ids, unary);
             continue;
         }
         // Only a warp's first and last rows can be shared: one slot for each.
         const int slot = (r == r_first) ? 0 : 1;
-        partials[(gw * 2 + slot) * 32 + lane] = L.e;
+        partials[((long long)gw * 2 + slot) * 32 + lane] = L.e;
         __threadfence();
         __syncwarp();
         unsigned arrived = 0;
@@ -333,11 +339,11 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
         if (arrived != (unsigned)(w1 - w0)) continue;   // not the last one: done
         __threadfence();
         uint64_t m = L.e;
-        for (long long w = w0; w <= w1; ++w) {
+        for (int w = w0; w <= w1; ++w) {
             if (w == gw) continue;
-            const int ws = (r == (w * span) / V) ? 0 : 1;
-            const uint64_t other = __ldcg(
-                reinterpret_cast<const unsigned long long*>(partials) + (w * 2 + ws) * 32 + lane);
+            const int ws = (r == (int)(((long long)w * span) / V)) ? 0 : 1;
+            const uint64_t other = __ldcg(reinterpret_cast<const unsigned long long*>(partials) +
+                                          ((long long)w * 2 + ws) * 32 + lane);
             m = merge_lists(m, other, lane);
         }
         write_row(m, r, lane, K, softcap, scale, cand_ids, unary);
@@ -353,8 +359,8 @@ int resident_blocks_per_sm(int device, int variant) {
     if (cache[device][variant] == 0) {
         int n = 0;
         cudaError_t e = variant == 0
-            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_kernel<3>, kThreads, 0)
-            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_kernel<2>, kThreads, 0);
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_kernel<3, kUnroll>, kThreads, 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_kernel<2, kUnroll>, kThreads, 0);
         if (e != cudaSuccess || n < 1) {
             (void)cudaGetLastError();
             n = 1;
@@ -417,11 +423,11 @@ cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
     cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
     if (err != cudaSuccess) return err;
     if (plan.variant == 0)
-        topk_kernel<3><<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span,
+        topk_kernel<3, kUnroll><<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span,
                                                              plan.warps, V, K, softcap, scale,
                                                              cand_ids, unary, counters, partials);
     else
-        topk_kernel<2><<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span,
+        topk_kernel<2, kUnroll><<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span,
                                                              plan.warps, V, K, softcap, scale,
                                                              cand_ids, unary, counters, partials);
     return cudaGetLastError();
