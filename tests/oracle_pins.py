@@ -354,6 +354,21 @@ def pin_edges_rank1(orc, seed: int = 9) -> None:
                     assert e[r, p, q, c] == want
 
 
+def pin_edges_subnormal_products(orc) -> None:
+    """Closed form with subnormal codebook entries: pred = 2^-130 (a bf16 subnormal), h = 2^100,
+    succ = 2^20, so every term is 2^-10 and every score is rank * 2^-10 exactly. A flush of
+    subnormal inputs, or a product taken in a format without them, gives 0 instead."""
+    R, S, K, V, rank = 2, 3, 2, 4, 16
+    pred = np.full((V, rank), 0x0008, dtype=np.uint16)       # 8 * 2^-133
+    succ = np.full((V, rank), 0x4980, dtype=np.uint16)       # exponent 147: 2^20
+    h = np.full((R, S, rank), 0x7180, dtype=np.uint16)       # exponent 227: 2^100
+    assert bits_to_float(pred)[0, 0] == np.float32(2.0 ** -130)
+    cand = np.array([[[0, 1], [2, 3], [1, 2]], [[3, 2], [1, 0], [0, 3]]], dtype=np.int32)
+    e = orc.edges(pred, succ, cand, np.zeros((R, S, K), np.float32), h,
+                  np.array([1, 2], dtype=np.int32))
+    assert np.all(e == np.float32(rank * 2.0 ** -10)), e
+
+
 def pin_edges_structure(orc, seed: int = 10) -> None:
     """At p = 0 every predecessor row is the same (the anchor). For p > 0, row q depends
     only on cand[r, p-1, q]: equal predecessors give equal rows, and changing the
@@ -523,8 +538,8 @@ ALL_PINS = [
     pin_topk_logits_processor_golden, pin_topk_logits_processor_vs_numpy,
     pin_bf16_round_cases, pin_bf16_round_vs_torch, pin_bf16_round_nearest,
     pin_projection_golden, pin_projection_closed_forms, pin_projection_vs_numpy,
-    pin_edges_golden, pin_edges_zero_codebooks, pin_edges_rank1, pin_edges_structure,
-    pin_edges_vs_einsum, pin_selector_composes, pin_lmhead_topk_vs_numpy,
+    pin_edges_golden, pin_edges_zero_codebooks, pin_edges_rank1, pin_edges_subnormal_products,
+    pin_edges_structure, pin_edges_vs_einsum, pin_selector_composes, pin_lmhead_topk_vs_numpy,
     pin_lmhead_topk_one_hot, pin_best_path_golden, pin_best_path_bruteforce,
     pin_best_path_independent_steps, pin_best_path_single_candidate,
 ]
