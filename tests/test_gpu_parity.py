@@ -671,6 +671,41 @@ def test_lmhead_topk_logits_processor(dev):
                           "lm head with soft cap", softcap=5.0, scale=0.5)
 
 
+def test_lmhead_odd_k_request_slices(dev):
+    """With K odd, request slices of the candidate ids, unary values and edge scores start off
+    16-byte boundaries (4-byte alignment is all they need). The LM-head top-k and the draft
+    step from the LM head, writing into such slices, equal the calls on whole arrays bit for
+    bit: each output's arithmetic does not depend on where its row sits in a tile."""
+    R, S, K, V, H, rank = 5, 3, 7, 3001, 128, 16
+    g = torch.Generator().manual_seed(77)
+    hid = _bf16(torch.randn(R, S, H, generator=g)).to(dev)
+    lm = _bf16(torch.randn(V, H, generator=g) / H ** 0.5).to(dev)
+    wp = _bf16(torch.randn(rank, H, generator=g) / H ** 0.5).to(dev)
+    pc = _bf16(torch.randn(V, rank, generator=g) / rank ** 0.5).to(dev)
+    sc = _bf16(torch.randn(V, rank, generator=g) / rank ** 0.5).to(dev)
+    anchors = torch.randint(0, V, (R,), generator=g, dtype=torch.int32).to(dev)
+    a, b = 1, 4
+    ids, un = ds.dflash_lmhead_topk(hid, lm, K)
+    s_ids, s_un = torch.zeros_like(ids), torch.zeros_like(un)
+    ds.dflash_lmhead_topk(hid[a:b], lm, K, s_ids[a:b], s_un[a:b])
+    torch.cuda.synchronize(dev)
+    assert s_ids[a:b].data_ptr() % 16 != 0
+    assert torch.equal(s_ids[a:b], ids[a:b])
+    assert torch.equal(s_un[a:b].view(torch.int32), un[a:b].view(torch.int32))
+    f_ids, f_un, f_h, f_e = ds.dflash_selector_lmhead(hid, lm, wp, pc, sc, anchors, K)
+    o_ids, o_un = torch.zeros_like(f_ids), torch.zeros_like(f_un)
+    o_h, o_e = torch.zeros_like(f_h), torch.zeros_like(f_e)
+    ds.dflash_selector_lmhead(hid[a:b], lm, wp, pc, sc, anchors[a:b], K, o_ids[a:b], o_un[a:b],
+                              o_h[a:b], o_e[a:b])
+    torch.cuda.synchronize(dev)
+    assert o_e[a:b].data_ptr() % 16 != 0
+    assert torch.equal(o_ids[a:b], f_ids[a:b])
+    assert torch.equal(o_un[a:b].view(torch.int32), f_un[a:b].view(torch.int32))
+    assert torch.equal(o_h[a:b].view(torch.int16), f_h[a:b].view(torch.int16))
+    assert torch.equal(o_e[a:b].view(torch.int32), f_e[a:b].view(torch.int32))
+    _status_clean()
+
+
 @pytest.mark.parametrize("R,S,K,V,H,rank,cap,scale", [
     (3, 7, 8, 5000, 256, 64, 0.0, 1.0),        # 21 rows, 20 vocabulary splits
     (40, 15, 32, 6000, 128, 128, 30.0, 1.5),   # 600 rows in 5 row tiles, K = 32, processed
