@@ -91,6 +91,10 @@ MUTANTS = [
     ("edges_sign_flipped",
      "s += bf16_to_double(a[j]) * bf16_to_double(hp[j]) * bf16_to_double(b[j]);",
      "s -= bf16_to_double(a[j]) * bf16_to_double(hp[j]) * bf16_to_double(b[j]);"),
+    ("edges_subnormal_codebook_flushed",
+     "s += bf16_to_double(a[j]) * bf16_to_double(hp[j]) * bf16_to_double(b[j]);",
+     "s += (fabs(bf16_to_double(a[j])) < 0x1p-126 ? 0.0 : bf16_to_double(a[j])) * "
+     "bf16_to_double(hp[j]) * bf16_to_double(b[j]);"),
     ("edges_h_dropped",
      "s += bf16_to_double(a[j]) * bf16_to_double(hp[j]) * bf16_to_double(b[j]);",
      "s += bf16_to_double(a[j]) * bf16_to_double(b[j]);"),
