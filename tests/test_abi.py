@@ -2,6 +2,9 @@
 include/dflash.h declares, and rejects bad arguments before any CUDA call."""
 
 import ctypes
+import os
+import shutil
+import subprocess
 
 import pytest
 import torch
@@ -206,3 +209,44 @@ def test_candidate_selector_module_host_checks():
     assert sel.predecessor_codebook.dtype == torch.bfloat16
     with pytest.raises(NotImplementedError):
         ds.CandidateSelector(64, 100, 16, 4, device="cpu", params_dtype=torch.float16)
+
+
+_C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "dflash.h"
+
+int main(void) {
+    int32_t ids[4];
+    float unary[4], logits[8] = {0};
+    dflash_status s;
+    if (strcmp(dflash_status_string(DFLASH_INVALID_ARGUMENT), "DFLASH_INVALID_ARGUMENT") != 0)
+        return 2;
+    if (dflash_version() == NULL) return 3;
+    /* R = 0 is refused by the argument checks, before any CUDA call. */
+    s = dflash_topk_candidates(logits, 0, 1, 8, 4, 0.0f, 1.0f, ids, unary, NULL, 0, NULL);
+    if (s != DFLASH_INVALID_ARGUMENT) return 4;
+    if (strlen(dflash_last_error()) == 0) return 5;
+    printf("%s\n", dflash_version());
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/dflash.h is a C99 header: a C program compiles against it with warnings as
+    errors, links the library, and gets the documented answers (no GPU needed)."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi.c"
+    src.write_text(_C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(_native._build.LIBRARY)
+    include = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", include,
+                    str(src), "-L", libdir, "-ldflash_gb300", f"-Wl,-rpath,{libdir}", "-o",
+                    str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.strip() == lib.dflash_version().decode()
