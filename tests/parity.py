@@ -105,24 +105,11 @@ def assert_projection(gpu_bits: np.ndarray, hidden_bits: np.ndarray, w_bits: np.
     assert rms_rel <= 2.0 ** -9, f"{what}: RMS error above half a bf16 step; {stats}"
 
 
-def oracle_topk_rows(logits: np.ndarray, K: int, rows: np.ndarray):
-    """Oracle top-k of selected flat rows of logits [R, S, V]."""
-    flat = logits.reshape(-1, logits.shape[-1])
-    return oracle.topk(flat[rows], K)
-
-
 def sample_rows(n_rows: int, k: int, seed: int, extra=()) -> np.ndarray:
     rng = np.random.default_rng(seed)
     pick = set(int(x) for x in rng.choice(n_rows, size=min(k, n_rows), replace=False))
     pick.update([0, n_rows - 1, n_rows // 2])
     pick.update(int(x) for x in extra if 0 <= x < n_rows)
-    return np.array(sorted(pick), dtype=np.int64)
-
-
-def sample_requests(R: int, k: int, seed: int) -> np.ndarray:
-    rng = np.random.default_rng(seed)
-    pick = set(int(x) for x in rng.choice(R, size=min(k, R), replace=False))
-    pick.update([0, R - 1])
     return np.array(sorted(pick), dtype=np.int64)
 
 

@@ -1,11 +1,14 @@
 """GPU parity: the sm_103a kernels, called through the C ABI, against the CPU oracle on
 the same seeded inputs.
 
-Small workloads are compared in full. The large ones (qwen_zipf, gemma_softcap,
-gemma_large) run at full size, in the launch configuration the benchmark times, and are
-compared on sampled rows or requests that the oracle computes one by one. Edge cases
-cover ragged sizes (V, H and rank not multiples of the tile sizes), exact ties, signed
-zeros, infinities, NaNs, sorted rows, K = 1, K = V, K = 32, step 0 only, and bad ids.
+Every workload is compared in full, the large ones (qwen_zipf, gemma_softcap, gemma_large)
+included: they run at full size, in the launch configuration the benchmark times, and every
+row, request and edge score is compared with the oracle's. The oracle's top-k and
+projection of a workload are computed once and reused by the tests that need them. Besides,
+a check that needs no oracle runs on the device over every row of the large workloads:
+exactly K - 1 logits beat the K-th candidate in the candidate order. Edge cases cover ragged
+sizes (V, H and rank not multiples of the tile sizes), exact ties, signed zeros, infinities,
+NaNs, sorted rows, K = 1, K = V, K = 32, step 0 only, and bad ids.
 """
 
 from __future__ import annotations
@@ -56,6 +59,48 @@ def _status_clean():
     assert ds.dflash_device_status(clear=True) == 0
 
 
+_ORACLE: dict = {}
+
+
+def oracle_topk_of(name):
+    """The oracle's top-k of a workload's logits (every row), computed once."""
+    inp = host_inputs(name)
+    key = ("topk", inp.workload.name)
+    if key not in _ORACLE:
+        _ORACLE[key] = oracle.topk(inp.logits, inp.workload.K)
+    return _ORACLE[key]
+
+
+def oracle_h_of(name):
+    """The oracle's projection of a workload's hidden states (every row), computed once."""
+    inp = host_inputs(name)
+    key = ("h", inp.workload.name)
+    if key not in _ORACLE:
+        _ORACLE[key] = oracle.projection(P.bits(inp.hidden), P.bits(inp.w_proj))
+    return _ORACLE[key]
+
+
+def assert_rank_of_kth(x: torch.Tensor, ids: torch.Tensor, K: int, what: str) -> None:
+    """On the device, for every row: exactly K - 1 logits come before the K-th candidate in
+    the candidate order (logit descending, then id ascending; -0 == +0). With distinct ids
+    in descending order this says the candidates are the row's top K, ties included. It
+    needs no oracle. Rows go in chunks so the temporaries stay near 1 GB."""
+    V = x.shape[-1]
+    x2, i2 = x.reshape(-1, V), ids.reshape(-1, K)
+    col = torch.arange(V, device=x.device, dtype=torch.int64)[None, :]
+    step = max(1, (1 << 28) // V)
+    for r0 in range(0, x2.shape[0], step):
+        xs = x2[r0:r0 + step]
+        kid = i2[r0:r0 + step, K - 1].long()[:, None]
+        kv = torch.gather(xs, 1, kid)
+        before = ((xs > kv) | ((xs == kv) & (col < kid))).sum(dim=1)
+        bad = torch.nonzero(before != K - 1)
+        if bad.numel():
+            r = int(bad[0, 0]) + r0
+            raise AssertionError(f"{what}: row {r} has {int(before[r - r0])} logits before its "
+                                 f"K-th candidate, not {K - 1}")
+
+
 # ----------------------------------------------------------------------------- top-k
 
 @pytest.mark.parametrize("name", SMALL + ["ragged"])
@@ -71,19 +116,18 @@ def test_topk_small_full(dev, name):
 
 
 @pytest.mark.parametrize("name", LARGE)
-def test_topk_large_sampled(dev, name):
+def test_topk_large_full(dev, name):
+    """Every row of the large workloads against the oracle: ids bit-exact, unary within
+    tolerance. Then, on the device, properties that need no oracle: distinct ids in range,
+    unary equal to the logit at the id, non-increasing unary, and the rank of the K-th
+    candidate."""
     inp = host_inputs(name)
     w = inp.workload
     x = torch.from_numpy(inp.logits).to(dev)
     ids, un = ds.dflash_topk_candidates(x, w.K)
-    rows = P.sample_rows(w.rows, 40, seed=1)
-    ref_ids, ref_un = P.oracle_topk_rows(inp.logits, w.K, rows)
-    got_ids = ids.reshape(w.rows, w.K)[torch.from_numpy(rows).to(dev)].cpu().numpy()
-    got_un = un.reshape(w.rows, w.K)[torch.from_numpy(rows).to(dev)].cpu().numpy()
-    P.assert_ids_equal(got_ids, ref_ids, f"{name} ids")
-    P.assert_close(got_un, ref_un, f"{name} unary")
-    # Properties that hold at any size, on every row: distinct ids in range, unary equal
-    # to the logit at the id, and non-increasing unary.
+    ref_ids, ref_un = oracle_topk_of(name)
+    P.assert_ids_equal(ids.cpu().numpy(), ref_ids, f"{name} ids")
+    P.assert_close(un.cpu().numpy(), ref_un, f"{name} unary")
     ids_all = ids.reshape(w.rows, w.K)
     assert int(ids_all.min()) >= 0 and int(ids_all.max()) < w.V
     srt = torch.sort(ids_all, dim=1).values
@@ -91,6 +135,7 @@ def test_topk_large_sampled(dev, name):
     gathered = torch.gather(x.reshape(w.rows, w.V), 1, ids_all.long())
     assert torch.equal(gathered, un.reshape(w.rows, w.K))
     assert bool((un[..., 1:] <= un[..., :-1]).all())
+    assert_rank_of_kth(x, ids, w.K, f"{name} rank of the K-th candidate")
     del x
     _status_clean()
 
@@ -183,14 +228,7 @@ def test_projection_workloads(dev, name):
     inp = host_inputs(RAGGED if name == "ragged" else name)
     w = inp.workload
     h = ds.dflash_hidden_projection(inp.hidden.to(dev), inp.w_proj.to(dev))
-    if name in LARGE:
-        rows = P.sample_rows(w.rows, 64, seed=2, extra=range(120, 140))
-        hid = P.bits(inp.hidden).reshape(w.rows, w.H)[rows]
-        got = P.bits(h).reshape(w.rows, w.rank)[rows]
-    else:
-        hid = P.bits(inp.hidden)
-        got = P.bits(h)
-    P.assert_projection(got, hid, P.bits(inp.w_proj), f"{name} h")
+    P.assert_projection(P.bits(h), P.bits(inp.hidden), P.bits(inp.w_proj), f"{name} h")
     _status_clean()
 
 
@@ -207,15 +245,10 @@ def test_projection_closed_forms(dev):
 
 # ----------------------------------------------------------------------------- edges
 
-def _edge_inputs_from_oracle(inp: wl.Inputs, req: np.ndarray | None = None):
+def _edge_inputs_from_oracle(name):
     """Candidates, unary and h from the ORACLE, so the edge kernel is tested alone."""
-    w = inp.workload
-    logits = inp.logits if req is None else inp.logits[req]
-    hid = P.bits(inp.hidden) if req is None else P.bits(inp.hidden)[req]
-    anchors = inp.anchors if req is None else inp.anchors[req]
-    ids, un = oracle.topk(logits, w.K)
-    h = oracle.projection(hid, P.bits(inp.w_proj))
-    return ids, un, h, anchors
+    ids, un = oracle_topk_of(name)
+    return ids, un, oracle_h_of(name), host_inputs(name).anchors
 
 
 def _run_edges(dev, inp, ids, un, h, anchors):
@@ -227,9 +260,9 @@ def _run_edges(dev, inp, ids, un, h, anchors):
 
 @pytest.mark.parametrize("name", SMALL + ["ragged"] + LARGE)
 def test_edges_workloads(dev, name):
-    inp = host_inputs(RAGGED if name == "ragged" else name)
-    req = P.sample_requests(inp.workload.R, 3, seed=3) if name in LARGE else None
-    ids, un, h, anchors = _edge_inputs_from_oracle(inp, req)
+    key = RAGGED if name == "ragged" else name
+    inp = host_inputs(key)
+    ids, un, h, anchors = _edge_inputs_from_oracle(key)
     e = _run_edges(dev, inp, ids, un, h, anchors)
     ref = oracle.edges(P.bits(inp.pred_cb), P.bits(inp.succ_cb), ids, un, h, anchors)
     P.assert_close(e.cpu().numpy(), ref, f"{name} edges")
@@ -344,34 +377,32 @@ def test_edges_many_waves_with_bad_ids(dev, R, S, K, V, rank):
 
 # ----------------------------------------------------------------------------- fused selector
 
-def _selector_check(dev, inp: wl.Inputs, req: np.ndarray | None, what: str):
+def _selector_check(dev, inp: wl.Inputs, what: str):
+    """The fused call on a whole workload against the oracle's own fused selector (every
+    request, row and edge score)."""
     w = inp.workload
     d = P.to_device(inp, dev)
     ids, un, h, e = ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"],
                                        d["succ_cb"], d["anchors"], w.K)
-    sel = slice(None) if req is None else torch.from_numpy(req).to(dev)
-    logits = inp.logits if req is None else inp.logits[req]
-    hid = P.bits(inp.hidden) if req is None else P.bits(inp.hidden)[req]
-    anchors = inp.anchors if req is None else inp.anchors[req]
-    r_ids, r_un, r_h, r_e = oracle.selector(logits, hid, P.bits(inp.w_proj), P.bits(inp.pred_cb),
-                                            P.bits(inp.succ_cb), anchors, w.K)
-    P.assert_ids_equal(ids[sel].cpu().numpy(), r_ids, f"{what} ids")
-    P.assert_close(un[sel].cpu().numpy(), r_un, f"{what} unary")
-    P.assert_projection(P.bits(h[sel]), hid, P.bits(inp.w_proj), f"{what} h")
-    P.assert_close(e[sel].cpu().numpy(), r_e, f"{what} edges")
+    r_ids, r_un, r_h, r_e = oracle.selector(inp.logits, P.bits(inp.hidden), P.bits(inp.w_proj),
+                                            P.bits(inp.pred_cb), P.bits(inp.succ_cb),
+                                            inp.anchors, w.K)
+    P.assert_ids_equal(ids.cpu().numpy(), r_ids, f"{what} ids")
+    P.assert_close(un.cpu().numpy(), r_un, f"{what} unary")
+    P.assert_projection(P.bits(h), P.bits(inp.hidden), P.bits(inp.w_proj), f"{what} h")
+    P.assert_close(e.cpu().numpy(), r_e, f"{what} edges")
     del d
     _status_clean()
 
 
 @pytest.mark.parametrize("name", SMALL + ["ragged"])
 def test_selector_small_full(dev, name):
-    _selector_check(dev, host_inputs(RAGGED if name == "ragged" else name), None, name)
+    _selector_check(dev, host_inputs(RAGGED if name == "ragged" else name), name)
 
 
 @pytest.mark.parametrize("name", LARGE)
-def test_selector_large_sampled(dev, name):
-    inp = host_inputs(name)
-    _selector_check(dev, inp, P.sample_requests(inp.workload.R, 2, seed=4), name)
+def test_selector_large_full(dev, name):
+    _selector_check(dev, host_inputs(name), name)
 
 
 def test_selector_trace(dev):
