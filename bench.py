@@ -1,7 +1,7 @@
 """Benchmark of the GB300 DFlash2 candidate selector.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--e2e-steps E] [--no-cpu-baseline]
+                    [--workload NAME] [--e2e-steps E] [--no-cpu-baseline] [--no-per-workload]
 
 One step is one dflash_selector call over one batch of the workload: vocabulary top-k,
 hidden projection and edge scores, with every input already in HBM. The default
@@ -17,7 +17,13 @@ Rank 0 prints one JSON line. It holds:
   * e2e: the same metric through the C ABI with pinned host buffers, host-to-device and
     device-to-host copies inside the timed region;
   * cpu_baseline: the CPU oracle, as it stands, on a bounded sample of the workload;
-  * clocks: nvidia-smi samples taken during the timed region.
+  * clocks: nvidia-smi samples taken during the timed region;
+  * forward (one GPU): the selector's forward pass on the step's candidates (projection,
+    then edges, the pages' DFlash2BeamCandidateSelector.forward), and each kernel alone,
+    with L2 flushed before every call;
+  * per_workload (one GPU): each of the other four workloads through the same call, after
+    the headline's timed region: step time, the top-k's and the whole step's fraction of
+    the HBM peak, and the CPU oracle timed over the whole workload.
 With torchrun (N > 1) every rank runs an independent replica on its own GPU and its own
 seed (weak scaling). The only collectives are a barrier and a max over ranks of the time.
 
@@ -81,8 +87,10 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
-    return {"hbm_gbs": 6800.0, "source": "fallback (6.8 TB/s, earlier GB300 measurement)"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "source": "fallback (6.8 TB/s and 1.9 PFLOP/s bf16, earlier GB300 measurement)"}
 
 
 def profiled_traffic(workload: wl.Workload) -> float | None:
@@ -205,6 +213,140 @@ def base_config(w: wl.Workload, world: int) -> dict:
             "rank": w.rank, "description": w.description,
             "l2": "inputs larger than L2 (no flush needed)",
             "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
+
+
+def l2_bytes(dev) -> int:
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        return 129 << 20
+
+
+def timed_calls(fn, steps: int, stream, flush: torch.Tensor | None) -> float:
+    """Mean ms of one call of fn over `steps` calls, timed with CUDA events on `stream`.
+
+    With a flush buffer (larger than L2), the buffer is rewritten before every call and each
+    call is timed alone, so no call finds its inputs in L2; otherwise the calls run back to
+    back between two events.
+    """
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+    pairs = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in pairs)
+
+
+def oracle_whole(inp: wl.Inputs) -> dict:
+    """The CPU oracle, as it stands, over the whole workload on all host cores."""
+    import oracle
+    w = inp.workload
+    threads = oracle.default_threads()
+    t = oracle_sample(inp, w.R, threads)
+    return {"value": w.edges_per_call / t, "unit": UNIT, "cores": min(threads, w.rows),
+            "kind": "oracle", "seconds": t,
+            "sample": f"all {w.R} requests x {w.S} steps of {w.name} (fp64 CPU oracle, {t:.2f} s)"}
+
+
+def measure_workload(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, seed: int,
+                     peak_gbs: float, with_cpu: bool) -> dict:
+    """One smaller workload through the same public call as the headline: step time, the
+    top-k's and the whole step's fraction of the HBM peak, and the oracle over all of it."""
+    inp = wl.make_inputs(w, seed=seed)
+    d = {"logits": torch.from_numpy(inp.logits).to(dev), "hidden": inp.hidden.to(dev),
+         "w_proj": inp.w_proj.to(dev), "pred_cb": inp.pred_cb.to(dev),
+         "succ_cb": inp.succ_cb.to(dev), "anchors": torch.from_numpy(inp.anchors).to(dev)}
+    cand = torch.empty((w.R, w.S, w.K), dtype=torch.int32, device=dev)
+    unary = torch.empty((w.R, w.S, w.K), dtype=torch.float32, device=dev)
+    h = torch.empty((w.R, w.S, w.rank), dtype=torch.bfloat16, device=dev)
+    edges = torch.empty((w.R, w.S, w.K, w.K), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.dflash_selector_workspace_bytes(w.R, w.S, w.V, w.K), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"], d["succ_cb"],
+                           d["anchors"], w.K, cand, unary, h, edges, ws)
+
+    b = w.algorithmic_bytes()
+    total = sum(b.values())
+    topk_bytes = b["logits"] + b["ids_unary_out"]
+    # Inputs within a few times the L2 would be partly served from it: flush between steps.
+    flush = (torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
+             if total < 3 * l2_bytes(dev) else None)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ds.dflash_trace_begin(steps)
+    ms = timed_calls(step, steps, stream, flush)
+    stages = ds.dflash_trace_end(steps)
+    topk_ms = statistics.mean(s[1] for s in stages)
+    out = {"R": w.R, "S": w.S, "K": w.K, "V": w.V, "H": w.H, "rank": w.rank,
+           "steps": steps, "ms_per_step": ms,
+           "value": w.edges_per_call / (ms / 1e3), "unit": UNIT,
+           "l2": ("L2 flushed before every step (a buffer of twice the L2 rewritten), each "
+                  "step timed alone" if flush is not None else "inputs larger than L2"),
+           "launch_mode": "eager",
+           "stages_ms": {"projection": statistics.mean(s[0] for s in stages), "topk": topk_ms,
+                         "edges": statistics.mean(s[2] for s in stages)},
+           "topk_hbm": {"algorithmic_bytes": topk_bytes,
+                        "achieved_gbs": topk_bytes / (topk_ms / 1e3) / 1e9,
+                        "frac": topk_bytes / (topk_ms / 1e3) / 1e9 / peak_gbs},
+           "fused_hbm": {"algorithmic_bytes_per_step": total,
+                         "achieved_gbs": total / (ms / 1e3) / 1e9,
+                         "frac": total / (ms / 1e3) / 1e9 / peak_gbs},
+           "device_status": ds.dflash_device_status(clear=True)}
+    del d, cand, unary, h, edges, ws, flush
+    torch.cuda.empty_cache()
+    if with_cpu:
+        out["cpu_baseline"] = oracle_whole(inp)
+    return out
+
+
+def measure_forward(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, peaks: dict, cand,
+                    unary, hidden, anchors, w_proj, pred_cb, succ_cb, h, edges) -> dict:
+    """The selector's forward pass on given candidates (projection, then edges), and each of
+    its two kernels alone, with L2 flushed before every call."""
+    flush = torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
+    calls = {
+        "forward": lambda: ds.dflash_selector_forward(cand, unary, hidden, anchors, w_proj,
+                                                      pred_cb, succ_cb, h, edges),
+        "projection": lambda: ds.dflash_hidden_projection(hidden, w_proj, h),
+        "edges": lambda: ds.dflash_candidate_edges(pred_cb, succ_cb, cand, unary, h, anchors,
+                                                   edges),
+    }
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(warmup):
+            fn()
+        out[f"{name}_ms"] = timed_calls(fn, steps, stream, flush)
+    b = w.algorithmic_bytes()
+    proj_bytes = b["hidden"] + b["w_proj"] + b["h_out"]
+    proj_flops = 2.0 * w.rows * w.H * w.rank
+    bound_ms = max(proj_bytes / (peaks["hbm_gbs"] * 1e9),
+                   proj_flops / (peaks["bf16_tflops"] * 1e12)) * 1e3
+    out["edge_scores_per_s"] = w.edges_per_call / (out["forward_ms"] / 1e3)
+    out["projection_roofline"] = {
+        "bound": "hbm" if proj_bytes / peaks["hbm_gbs"] > proj_flops / peaks["bf16_tflops"] / 1e3
+                 else "tensor",
+        "algorithmic_bytes": proj_bytes, "flops": proj_flops, "bound_ms": bound_ms,
+        "frac": bound_ms / out["projection_ms"],
+        "what": "max(bytes / HBM peak, FLOPs / bf16 burst peak), both measured, over the "
+                "projection's time"}
+    out["l2"] = "L2 flushed before every call (a buffer of twice the L2 rewritten)"
+    del flush
+    return out
 
 
 # ----------------------------------------------------------------------------- arms
@@ -429,8 +571,24 @@ def run_ours(args, w: wl.Workload) -> None:
             "device_status": status,
             "clocks": clocks.summary(),
         }
+        if world == 1 and not args.no_per_workload:
+            # The pages' DFlash2BeamCandidateSelector.forward on the step's own candidates.
+            line["forward"] = measure_forward(ds, w, dev, stream, args.steps, args.warmup, peaks,
+                                              cand, unary, hidden, anchors, w_proj, pred_cb,
+                                              succ_cb, h, edges)
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(inp)
+        if world == 1 and not args.no_per_workload:
+            # The other workloads through the same call: their own step times, HBM fractions
+            # and the oracle over each of them in full. Not part of the timed region above.
+            del logits, hidden, anchors, w_proj, pred_cb, succ_cb, cand, unary, h, edges, ws
+            del logits_host, hidden_host, anchors_host, inp
+            torch.cuda.empty_cache()
+            line["per_workload"] = {
+                name: measure_workload(ds, wl.WORKLOADS[name], dev, stream, args.steps,
+                                       args.warmup, rank, peaks["hbm_gbs"],
+                                       with_cpu=not args.no_cpu_baseline)
+                for name in wl.WORKLOAD_ORDER if name != w.name}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -628,6 +786,8 @@ def main(argv=None) -> None:
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="request chunks the end-to-end loop pipelines copies and kernels over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the forward pass and the other workloads after the headline")
     ap.add_argument("--lmhead", action="store_true",
                     help="time the candidate head straight from a synthetic LM head instead")
     ap.add_argument("--sustained", type=float, default=0.0,
