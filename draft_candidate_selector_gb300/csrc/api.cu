@@ -45,16 +45,27 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 __device__ uint32_t g_device_status;
 
 constexpr int kMaxDevices = 64;
+// Caller streams per device that get a side stream of their own in the fused selector.
+constexpr int kMaxSideStreams = 64;
+
+// The fused selector runs the projection on a side stream beside the top-k. Each caller
+// stream has its own, so a stream being captured into a graph never shares its side stream
+// (which joins the capture) with another caller's eager work.
+struct SideStream {
+    cudaStream_t caller = nullptr;
+    std::mutex mu;   // keeps the record/wait pairs of concurrent callers from interleaving
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join = nullptr;
+};
 
 struct DeviceSlot {
     dflash::DeviceInfo info;
     uint32_t* status_word = nullptr;
     bool ready = false;
-    // The fused selector runs the projection on this stream, beside the top-k.
-    std::mutex fork_mu;
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr;
-    cudaEvent_t join = nullptr;
+    std::mutex side_mu;   // guards n_side and the caller keys
+    int n_side = 0;
+    SideStream side[kMaxSideStreams];
 };
 
 std::mutex g_dev_mu;
@@ -95,17 +106,34 @@ dflash_status current_device(dflash::DeviceInfo* info, uint32_t** status_word) {
     return DFLASH_OK;
 }
 
-// The side stream and fork/join events of the current device, created on first use.
-dflash_status side_stream(int device, DeviceSlot** slot) {
-    DeviceSlot& s = g_dev[device];
-    std::lock_guard<std::mutex> lock(s.fork_mu);
-    if (!s.side) {
-        cudaError_t e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cuda_fail(e, "creating the selector's side stream");
+// The side stream and fork/join events of a caller stream on the current device, created on
+// the first fused call from that stream. *out is nullptr once kMaxSideStreams caller streams
+// have one: the projection then runs on the caller's stream, before the top-k.
+dflash_status side_stream(int device, cudaStream_t caller, SideStream** out) {
+    DeviceSlot& d = g_dev[device];
+    std::lock_guard<std::mutex> lock(d.side_mu);
+    *out = nullptr;
+    for (int i = 0; i < d.n_side; ++i)
+        if (d.side[i].caller == caller) {
+            *out = &d.side[i];
+            return DFLASH_OK;
+        }
+    if (d.n_side == kMaxSideStreams) return DFLASH_OK;
+    SideStream& s = d.side[d.n_side];
+    cudaError_t e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        if (s.join) cudaEventDestroy(s.join);
+        if (s.fork) cudaEventDestroy(s.fork);
+        if (s.side) cudaStreamDestroy(s.side);
+        s.side = nullptr;
+        s.fork = s.join = nullptr;
+        return cuda_fail(e, "creating the selector's side stream");
     }
-    *slot = &s;
+    s.caller = caller;
+    ++d.n_side;
+    *out = &s;
     return DFLASH_OK;
 }
 
@@ -395,26 +423,32 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
         return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
                     workspace_bytes, plan.workspace_bytes());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    DeviceSlot* slot = nullptr;
-    DFLASH_TRY(side_stream(dev.device, &slot));
+    SideStream* side = nullptr;
+    DFLASH_TRY(side_stream(dev.device, st, &side));
     cudaEvent_t* ev = trace_slot(dev.device);
     // The projection does not depend on the top-k, and one projection CTA per SM fits
-    // beside the top-k's: fork it onto the side stream, join before the edges. The lock
-    // keeps the record/wait pairs of concurrent callers from interleaving.
-    std::lock_guard<std::mutex> lock(slot->fork_mu);
+    // beside the top-k's: fork it onto the caller stream's side stream, join before the
+    // edges. Without a side stream it runs first on the caller's stream.
+    std::unique_lock<std::mutex> lock;
+    if (side) lock = std::unique_lock<std::mutex>(side->mu);
+    const cudaStream_t proj_st = side ? side->side : st;
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    if ((e = cudaEventRecord(slot->fork, st)) != cudaSuccess) return cuda_fail(e, "fork event");
-    if ((e = cudaStreamWaitEvent(slot->side, slot->fork, 0)) != cudaSuccess)
-        return cuda_fail(e, "fork wait");
-    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, slot->side);
+    if (side) {
+        if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess) return cuda_fail(e, "fork event");
+        if ((e = cudaStreamWaitEvent(side->side, side->fork, 0)) != cudaSuccess)
+            return cuda_fail(e, "fork wait");
+    }
+    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, proj_st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    if (ev && (e = cudaEventRecord(ev[1], slot->side)) != cudaSuccess) return cuda_fail(e, "trace event");
-    if ((e = cudaEventRecord(slot->join, slot->side)) != cudaSuccess) return cuda_fail(e, "join event");
+    if (ev && (e = cudaEventRecord(ev[1], proj_st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    if (side && (e = cudaEventRecord(side->join, side->side)) != cudaSuccess)
+        return cuda_fail(e, "join event");
     e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    if ((e = cudaStreamWaitEvent(st, slot->join, 0)) != cudaSuccess) return cuda_fail(e, "join wait");
+    if (side && (e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess)
+        return cuda_fail(e, "join wait");
     e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
                              rank, edges, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "edges launch");

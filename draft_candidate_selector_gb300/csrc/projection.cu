@@ -87,6 +87,7 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
 
     if (warp == 0 && lane == 0) {
         // TMA producer.
+        int issued = 0;
         for (int kb = 0; kb < num_kb; ++kb) {
             const int s = kb % kStages;
             if (kb >= kStages && !mbar_wait(smem_u32(&empty[s]), ((kb / kStages) - 1) & 1)) {
@@ -97,7 +98,13 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
             mbar_expect_tx(fb, kATileBytes + b_tile_bytes);
             tma_load_2d(smem_u32(sa + s * kATileBytes), &map_a, fb, kb * BK, m0);
             tma_load_2d(smem_u32(sb + s * b_tile_bytes), &map_b, fb, kb * BK, n0);
+            issued = kb + 1;
         }
+        // The last load into each stage must land before the CTA may leave and its shared
+        // memory be reused, also after a timeout. Each wait is bounded; in the normal case
+        // those loads were consumed long ago and every wait returns at once.
+        for (int q = issued > kStages ? issued - kStages : 0; q < issued; ++q)
+            (void)mbar_wait(smem_u32(&full[q % kStages]), (q / kStages) & 1);
     } else if (warp == 1 && lane == 0) {
         // MMA issuer.
         const uint32_t idesc = f16_idesc(BM, BN);
@@ -121,11 +128,6 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
         }
         // Signals once every MMA issued above has completed (also after a timeout).
         umma_commit(smem_u32(accum));
-        // After a timeout, wait (bounded) for TMA loads still in flight into the ring.
-        for (int k2 = kb + 1; k2 < num_kb && k2 < kb + kStages; ++k2) {
-            const int s = k2 % kStages;
-            if (!mbar_wait(smem_u32(&full[s]), (k2 / kStages) & 1)) break;
-        }
     }
     __syncwarp();
 

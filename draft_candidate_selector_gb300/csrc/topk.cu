@@ -379,21 +379,26 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 cudaError_t topk_static_scratch(int device, void** ptr) {
     // Host code only sees a stand-in for the array's name, so its device address is looked
-    // up once per device, with that device current (the caller makes it current).
+    // up per device, with that device current (the caller makes it current). Only a
+    // successful lookup is kept: a failed one (for example a first call made while the
+    // stream is capturing) is cleared from the thread's error state and tried again on the
+    // next call.
     static std::mutex mu;
     static void* addr[64] = {nullptr};
-    static cudaError_t err[64];
-    static bool done[64] = {false};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (!done[device]) {
+    if (!addr[device]) {
         void* p = nullptr;
-        err[device] = cudaGetSymbolAddress(&p, g_static_scratch);
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            *ptr = nullptr;
+            return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+        }
         addr[device] = p;
-        done[device] = true;
     }
     *ptr = addr[device];
-    return err[device];
+    return cudaSuccess;
 }
 
 TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V) {

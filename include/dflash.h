@@ -59,7 +59,7 @@ typedef enum {
     DFLASH_UNSUPPORTED = 2,         /* valid request outside the implemented envelope     */
     DFLASH_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the *_workspace_bytes query  */
     DFLASH_CUDA_ERROR = 4,          /* a CUDA runtime call or a launch failed             */
-    DFLASH_NO_DEVICE = 5            /* no usable sm_100-family device is current          */
+    DFLASH_NO_DEVICE = 5            /* the current device is not a GB300 (sm_103a), or none */
 } dflash_status;
 
 /* Bits of the device status word (dflash_device_status). */
@@ -118,7 +118,8 @@ dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, i
  * nothing; use dflash_topk_candidates with a workspace then.
  * - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  * - The first call on a device looks up the array's device address. Make that first call
- *   before any stream capture on the device.
+ *   before any stream capture on the device. A lookup that fails is not remembered: the
+ *   call returns DFLASH_CUDA_ERROR and the next call tries again.
  * - Every call on a device shares the one array. Each call clears the counters it needs
  *   (a memset on `stream`) before its kernel runs. Calls that overlap on the GPU (on
  *   different streams, or from several threads) race on the array: serialise them.
@@ -160,7 +161,9 @@ dflash_status dflash_lmhead_topk(const uint16_t* hidden, const uint16_t* lm_head
  * hidden  [R, S, H]    bf16   drafter hidden states
  * w_proj  [rank, H]    bf16   projection weight, in the Linear [out, in] convention
  * h_out   [R, S, rank] bf16   out: fp32 accumulation, rounded to bf16 (nearest-even)
- * Runs on the tensor cores (tcgen05, operands staged by TMA). Needs an sm_100-family GPU.
+ * Runs on the tensor cores (tcgen05, operands staged by TMA). Like every compute call of
+ * this library it needs a GB300 (compute capability 10.3): the library is built for
+ * sm_103a only, and other devices get DFLASH_NO_DEVICE.
  * ---------------------------------------------------------------------------------- */
 dflash_status dflash_hidden_projection(const uint16_t* hidden, const uint16_t* w_proj,
                                        int R, int S, int H, int rank, uint16_t* h_out,
@@ -192,10 +195,14 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
 /* ------------------------------------------------------------------------------------
  * The whole selector in one call, with no host round trip. Step 2 (projection) runs on a
  * library-owned side stream beside step 1 (top-k) on `stream`; step 3 (edges) follows
- * both on `stream`. The call returns once everything is enqueued; later work on `stream`
- * sees all outputs. It is safe to capture in a CUDA graph: the side stream joins the
- * capture through an event. The outputs, workspace, softcap and scale are as in the three
- * calls above; the edge scores use the processed unary values.
+ * both on `stream`. Each caller stream gets a side stream of its own, on its first fused
+ * call (up to 64 caller streams per device; beyond that the projection runs on `stream`
+ * itself, before the top-k). The call returns once everything is enqueued; later work on
+ * `stream` sees all outputs. It is safe to capture in a CUDA graph: the side stream joins
+ * the capture through an event, and since it belongs to the capturing stream alone, eager
+ * calls on other streams meanwhile stay out of the graph. Make one call on the device
+ * before capturing. The outputs, workspace, softcap and scale are as in the three calls
+ * above; the edge scores use the processed unary values.
  * Source: the draft step captures the candidate head and the selector together
  * (module docstring of the page).
  * ---------------------------------------------------------------------------------- */
