@@ -439,7 +439,8 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
         if ((e = cudaStreamWaitEvent(side->side, side->fork, 0)) != cudaSuccess)
             return cuda_fail(e, "fork wait");
     }
-    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, proj_st);
+    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, proj_st,
+                                  /*beside_topk=*/side != nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     if (ev && (e = cudaEventRecord(ev[1], proj_st)) != cudaSuccess) return cuda_fail(e, "trace event");
     if (side && (e = cudaEventRecord(side->join, side->side)) != cudaSuccess)

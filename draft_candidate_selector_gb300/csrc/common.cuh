@@ -57,9 +57,13 @@ cudaError_t topk_static_scratch(int device, void** ptr);
 
 // Returns cudaSuccess, or an error if the tensor maps cannot be encoded or the launch
 // fails. status_word receives kStatusTimeout if a bounded pipeline wait gives up.
+// beside_topk selects the build that keeps to 32 registers per thread, so that a projection
+// CTA fits on an SM beside three top-k CTAs (the fused selector's schedule); the results of
+// the two builds are identical.
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank,
-                              uint16_t* h_out, uint32_t* status_word, cudaStream_t stream);
+                              uint16_t* h_out, uint32_t* status_word, cudaStream_t stream,
+                              bool beside_topk = false);
 
 // ---------------------------------------------------------------- edges (edges.cu)
 

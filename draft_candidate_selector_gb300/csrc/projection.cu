@@ -8,19 +8,37 @@
 // GEMM view: D[M = R*S, N = rank] = A[M, K = H] . B[N, K]^T. A (hidden) and B (W_proj,
 // Linear [out, in]) are both K-major, which is the native operand form of tcgen05.mma.
 //
-// One CTA computes one 128 x BN tile of D, with BN = min(rank rounded up to 16, 128):
+// Tiling. The output is cut into 128 x BN tiles, BN = the rank rounded up to 16, at most
+// 128 (N tiles beyond the first re-read the same hidden-state tile, mostly from L2). A
+// cluster of `ks` CTAs computes one tile, splitting K: CTA s of the cluster (its cluster
+// rank) takes the contiguous K blocks [s * nkb / ks, (s + 1) * nkb / ks). The host doubles
+// ks, from 1, while the tiles times ks still fit the SMs in one wave and every split keeps
+// at least 8 K blocks (gemma_large: 60 x 2 tiles, ks = 1; gemma_softcap: 30 tiles, ks = 4;
+// qwen_zipf: 8 tiles, ks = 4). Each CTA's time is set by its chain of K blocks: a stage
+// makes a round trip (TMA load, MMAs, release) of about 1.7 us, with 6 stages in flight,
+// whatever the stage's bytes. In each CTA:
 //   * warp 0, one lane: TMA producer. Per 64-wide K block it loads a 128x64 A tile and a
-//     BNx64 B tile (128-byte swizzle) into a 6-stage shared-memory ring. Completion is
-//     tracked on mbarriers by transaction bytes.
+//     BNx64 B tile (128-byte swizzle) into a ring of `stages` shared-memory stages (6 at
+//     BN = 128, up to 8). Completion is tracked on mbarriers by transaction bytes.
 //   * warp 1, one lane: MMA issuer. tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), M=128,
-//     N=BN, K=16, four per K block, accumulating in tensor memory. tcgen05.commit
-//     frees each stage and finally signals the accumulator.
-//   * warps 0-3: epilogue. tcgen05.ld 32 lanes x 16 columns per warp, convert to bf16,
-//     store to global memory.
+//     N=BN, K=16, four per K block, accumulating in tensor memory. tcgen05.commit frees
+//     each stage and finally signals the accumulator.
+//   * warps 0-3: epilogue; thread t owns row t of the tile (tensor-memory lane t).
+//       ks = 1: tcgen05.ld 16 columns at a time (8 in the register-capped build), round
+//       to bf16, store.
+//       ks > 1: the tile's columns are cut into ks slices of BN / ks; CTA s owns slice s.
+//       Once every CTA's MMAs are done (cluster barrier), each CTA writes its fp32
+//       partials of the slices it does not own into the owners' shared memory
+//       (distributed shared memory, over the now idle ring), a second cluster barrier
+//       makes them visible, and each owner adds the ks partials of its slice in split
+//       order (0, 1, ...), rounds to bf16 and stores. The sum order is fixed, so the result
+//       does not depend on which CTA owns which slice.
 // Out-of-range rows, columns and K are zero-filled by TMA and never stored.
 // Every mbarrier wait is bounded, about one second by %globaltimer. On expiry the kernel
-// sets kStatusTimeout, skips the remaining work, still frees its tensor memory, and
-// returns.
+// sets kStatusTimeout, skips the remaining work, still takes part in both cluster
+// barriers, frees its tensor memory, and returns.
+// The fused selector runs the projection beside the top-k: its build keeps to 32 registers
+// per thread, so that one projection CTA (128 threads) fits beside three top-k CTAs on an SM.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -36,35 +54,50 @@ using namespace ptx;
 
 constexpr int BM = 128;
 constexpr int BK = 64;                 // bf16 elements in one 128-byte swizzle row
-constexpr int kStages = 6;
 constexpr int kThreads = 128;
 constexpr uint32_t kATileBytes = BM * BK * 2;
+constexpr uint32_t kRingBudget = 192u * 1024u;   // shared memory for the stage ring
+constexpr int kMaxStages = 8;
+constexpr int kMaxSplit = 8;
+constexpr int kMinKbPerSplit = 8;      // K blocks each split must keep
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Bytes of one receive row of a slice of `slice` fp32 columns, padded by 16 B so that the
+// owner's row-per-thread reads spread over the banks.
+__host__ __device__ constexpr uint32_t recv_row_bytes(int slice) { return (uint32_t)slice * 4u + 16u; }
+
+// Two builds. kMinBlocks = 16 caps the registers at 32 per thread, so that one projection
+// CTA fits beside three top-k CTAs on an SM (the fused selector runs them side by side);
+// kMinBlocks = 1 leaves the compiler free, for calls where nothing runs beside it.
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                   uint16_t* __restrict__ out, int M, int N, int Kdim, int BN, uint32_t tmem_cols,
-                  uint32_t* __restrict__ status) {
+                  int ks, int stages, uint32_t* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
-    // The 128-byte swizzle pattern repeats every 1024 B: tiles start on that boundary.
+    // The 128-byte swizzle pattern repeats every 1024 B: tiles start on that boundary. Every
+    // CTA has the same layout, so an offset names the same place in each CTA of a cluster.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t b_tile_bytes = (uint32_t)BN * BK * 2;
     uint8_t* sa = smem;
-    uint8_t* sb = smem + kStages * kATileBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + kStages * b_tile_bytes);
-    uint64_t* full = bars;                  // [kStages] TMA landed
-    uint64_t* empty = bars + kStages;       // [kStages] MMAs done reading
-    uint64_t* accum = bars + 2 * kStages;   // all MMAs done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+    uint8_t* sb = smem + stages * kATileBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + stages * b_tile_bytes);
+    uint64_t* full = bars;                  // [stages] TMA landed
+    uint64_t* empty = bars + stages;        // [stages] MMAs done reading
+    uint64_t* accum = bars + 2 * stages;    // all MMAs done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM;
+    const int split = ks > 1 ? (int)cluster_ctarank() : 0;
+    const int m0 = (blockIdx.x / ks) * BM;
     const int n0 = blockIdx.y * BN;
-    const int num_kb = (Kdim + BK - 1) / BK;
+    const int nkb = (Kdim + BK - 1) / BK;
+    const int kb0 = split * nkb / ks;
+    const int n_kb = (split + 1) * nkb / ks - kb0;   // >= 1: the host keeps ks <= nkb
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -87,31 +120,33 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
 
     if (warp == 0 && lane == 0) {
         // TMA producer.
+        // The stage and its phase advance with the K block (no division on the way).
         int issued = 0;
-        for (int kb = 0; kb < num_kb; ++kb) {
-            const int s = kb % kStages;
-            if (kb >= kStages && !mbar_wait(smem_u32(&empty[s]), ((kb / kStages) - 1) & 1)) {
+        for (int i = 0, s = 0, ph = 0; i < n_kb; ++i) {
+            if (i >= stages && !mbar_wait(smem_u32(&empty[s]), ph ^ 1)) {
                 atomicOr(status, kStatusTimeout);
                 break;
             }
             const uint32_t fb = smem_u32(&full[s]);
             mbar_expect_tx(fb, kATileBytes + b_tile_bytes);
-            tma_load_2d(smem_u32(sa + s * kATileBytes), &map_a, fb, kb * BK, m0);
-            tma_load_2d(smem_u32(sb + s * b_tile_bytes), &map_b, fb, kb * BK, n0);
-            issued = kb + 1;
+            tma_load_2d(smem_u32(sa + s * kATileBytes), &map_a, fb, (kb0 + i) * BK, m0);
+            tma_load_2d(smem_u32(sb + s * b_tile_bytes), &map_b, fb, (kb0 + i) * BK, n0);
+            issued = i + 1;
+            if (++s == stages) {
+                s = 0;
+                ph ^= 1;
+            }
         }
-        // The last load into each stage must land before the CTA may leave and its shared
-        // memory be reused, also after a timeout. Each wait is bounded; in the normal case
-        // those loads were consumed long ago and every wait returns at once.
-        for (int q = issued > kStages ? issued - kStages : 0; q < issued; ++q)
-            (void)mbar_wait(smem_u32(&full[q % kStages]), (q / kStages) & 1);
+        // The last load into each stage must land before the CTA may leave, or its ring be
+        // reused for the partial sums, also after a timeout. Each wait is bounded; in the
+        // normal case those loads were consumed long ago and every wait returns at once.
+        for (int q = issued > stages ? issued - stages : 0; q < issued; ++q)
+            (void)mbar_wait(smem_u32(&full[q % stages]), (q / stages) & 1);
     } else if (warp == 1 && lane == 0) {
         // MMA issuer.
         const uint32_t idesc = f16_idesc(BM, BN);
-        int kb = 0;
-        for (; kb < num_kb; ++kb) {
-            const int s = kb % kStages;
-            if (!mbar_wait(smem_u32(&full[s]), (kb / kStages) & 1)) {
+        for (int i = 0, s = 0, ph = 0; i < n_kb; ++i) {
+            if (!mbar_wait(smem_u32(&full[s]), ph)) {
                 atomicOr(status, kStatusTimeout);
                 break;
             }
@@ -122,9 +157,13 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
             for (int k = 0; k < BK / 16; ++k) {
                 // Advancing 16 bf16 (32 B) along K inside the swizzled 128-byte row.
                 umma_bf16(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
-                          (kb | k) != 0);
+                          (i | k) != 0);
             }
             umma_commit(smem_u32(&empty[s]));
+            if (++s == stages) {
+                s = 0;
+                ph ^= 1;
+            }
         }
         // Signals once every MMA issued above has completed (also after a timeout).
         umma_commit(smem_u32(accum));
@@ -134,29 +173,112 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     // Epilogue: every warp drains its 32 TMEM lanes (= 32 output rows).
     const bool ready = __all_sync(0xffffffffu, mbar_wait(smem_u32(accum), 0));
     tc_fence_after();
-    if (ready) {
-        const int row = m0 + warp * 32 + lane;
-        uint16_t* orow = out + (long long)row * N;
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-            const int col = n0 + c0;
-            if (row < M && col < N) {
-                uint4 w0, w1;
-                w0.x = pack_bf16x2(v[0], v[1]);
-                w0.y = pack_bf16x2(v[2], v[3]);
-                w0.z = pack_bf16x2(v[4], v[5]);
-                w0.w = pack_bf16x2(v[6], v[7]);
-                w1.x = pack_bf16x2(v[8], v[9]);
-                w1.y = pack_bf16x2(v[10], v[11]);
-                w1.z = pack_bf16x2(v[12], v[13]);
-                w1.w = pack_bf16x2(v[14], v[15]);
-                reinterpret_cast<uint4*>(orow + col)[0] = w0;          // N % 8 == 0
-                if (col + 8 < N) reinterpret_cast<uint4*>(orow + col)[1] = w1;
+    if (!ready && lane == 0) atomicOr(status, kStatusTimeout);
+    const int trow = warp * 32 + lane;          // row of the tile, and its tensor-memory lane
+    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+    if (ks == 1) {
+        if (ready) {
+            // Columns past N (the rank rounded up to 16) are loaded and dropped; N % 8 == 0,
+            // so each 8-column piece is all in or all out.
+            const int cols = min(BN, N - n0);
+            uint4* orow = reinterpret_cast<uint4*>(out + (long long)(m0 + trow) * N + n0);
+            const bool live = m0 + trow < M;
+            if constexpr (kMinBlocks == 1) {
+                // 16 columns per tensor-memory load: one wait per 16.
+                for (int c0 = 0; c0 < cols; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tlane + (uint32_t)c0, v);
+                    if (live) {
+                        orow[c0 >> 3] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                        if (c0 + 8 < cols)
+                            orow[(c0 >> 3) + 1] =
+                                make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
+                                           pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+                    }
+                }
+            } else {
+                // 8 columns per load: a 16-column load does not fit in 32 registers.
+                for (int c0 = 0; c0 < cols; c0 += 8) {
+                    uint32_t v[8];
+                    tmem_ld_32x32b_x8(tlane + (uint32_t)c0, v);
+                    if (live)
+                        orow[c0 >> 3] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                }
             }
         }
-    } else if (threadIdx.x == 0) {
-        atomicOr(status, kStatusTimeout);
+    } else {
+        // Receive area of this CTA, over its ring (idle from here on): slot j holds the
+        // partials of the j-th other CTA (in split order), one padded row per tile row.
+        // Barrier 1: every CTA of the cluster is done with its ring.
+        cluster_sync();
+        if (ready) {
+            const int me = (int)cluster_ctarank();
+            const int slice = BN / ks;               // a multiple of 16
+            const uint32_t rrow = recv_row_bytes(slice);
+            for (int o = 0; o < ks; ++o) {
+                if (o == me) continue;
+                // In owner o's receive area, sender `me` uses slot me (or me - 1).
+                const uint32_t dst = mapa(smem_u32(smem) + (uint32_t)(me < o ? me : me - 1) *
+                                              (uint32_t)BM * rrow + (uint32_t)trow * rrow,
+                                          (uint32_t)o);
+                for (int c = 0; c < slice; c += 4) {
+                    uint32_t v[4];
+                    tmem_ld_32x32b_x4(tlane + (uint32_t)(o * slice + c), v);
+                    st_cluster_v4(dst + (uint32_t)c * 4u, v[0], v[1], v[2], v[3]);
+                }
+            }
+        }
+        // Barrier 2: the partials written to peers are visible to them.
+        cluster_sync();
+        if (ready) {
+            // Every lane runs the warp-wide tensor-memory loads; only rows < M are stored.
+            const int me = (int)cluster_ctarank();
+            const int slice = BN / ks;
+            const uint32_t rrow = recv_row_bytes(slice);
+            const uint8_t* rbase = smem + (size_t)trow * rrow;
+            for (int c = 0; c < slice; c += 8) {
+                const int col = me * slice + c;      // within the tile
+                if (n0 + col >= N) break;            // warp-uniform; N % 8 == 0
+                // This CTA's own partial (one load, one wait), then the sum in split order
+                // 0, 1, ...: acc = p0, then acc += p1, and so on.
+                uint32_t v[8];
+                tmem_ld_32x32b_x8(tlane + (uint32_t)col, v);
+                float acc[8];
+                if (me == 0) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = __uint_as_float(v[j]);
+                } else {
+                    const float4* q = reinterpret_cast<const float4*>(rbase + (size_t)c * 4);
+                    const float4 a = q[0], b = q[1];
+                    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+                    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+                }
+                for (int s = 1; s < ks; ++s) {
+                    if (s == me) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[j] += __uint_as_float(v[j]);
+                    } else {
+                        const float4* q = reinterpret_cast<const float4*>(
+                            rbase + (size_t)(s < me ? s : s - 1) * BM * rrow + (size_t)c * 4);
+                        const float4 a = q[0];
+                        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                        const float4 b = q[1];
+                        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+                    }
+                }
+                const int row = m0 + trow;
+                if (row < M) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
+                    w.y = pack_bf16x2(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
+                    w.z = pack_bf16x2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
+                    w.w = pack_bf16x2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
+                    *reinterpret_cast<uint4*>(out + (long long)row * N + n0 + col) = w;
+                }
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -205,36 +327,127 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int BN) {
-    return 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * BK * 2) +
-           (2 * kStages + 1) * sizeof(uint64_t) + 16;
+struct ProjPlan {
+    int BN = 0;             // N tile: the rank rounded up to 16, at most 128
+    uint32_t tmem_cols = 0; // power of two >= max(32, BN)
+    int stages = 0;         // ring stages
+    int ks = 1;             // K splits per tile = CTAs per cluster
+    int m_tiles = 0;
+    int n_tiles = 0;
+    size_t smem = 0;        // dynamic shared memory per CTA
+};
+
+uint32_t recv_bytes(int BN, int ks) {
+    return ks > 1 ? (uint32_t)(ks - 1) * BM * recv_row_bytes(BN / ks) : 0u;
+}
+
+size_t smem_bytes(int BN, int stages) {
+    return 1024 + (size_t)stages * (kATileBytes + (size_t)BN * BK * 2) +
+           (2 * stages + 1) * sizeof(uint64_t) + 16;
+}
+
+// Largest dynamic shared memory any plan asks for (set once per device).
+size_t max_smem_bytes() {
+    size_t m = 0;
+    for (int BN = 16; BN <= 128; BN += 16) {
+        const uint32_t stage = kATileBytes + (uint32_t)BN * BK * 2;
+        int st = (int)(kRingBudget / stage);
+        st = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
+        const size_t b = smem_bytes(BN, st);
+        m = b > m ? b : m;
+    }
+    return m;
+}
+
+// Whether clusters of ks CTAs of this kernel, with smem bytes each, can be resident.
+bool cluster_fits(int device, int ks, size_t smem) {
+    static std::mutex mu;
+    static int cache[64][kMaxSplit + 1] = {{0}};   // 0 unknown, 1 fits, 2 does not
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return false;
+    if (cache[device][ks] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)ks;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)ks);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, projection_kernel<16>, &cfg);
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        cache[device][ks] = (e == cudaSuccess && n > 0) ? 1 : 2;
+    }
+    return cache[device][ks] == 1;
+}
+
+ProjPlan projection_plan(const DeviceInfo& dev, int M, int H, int rank) {
+    ProjPlan p;
+    p.BN = rank >= 128 ? 128 : ((rank + 15) / 16) * 16;
+    p.n_tiles = (rank + p.BN - 1) / p.BN;
+    p.tmem_cols = 32;
+    while (p.tmem_cols < (uint32_t)p.BN) p.tmem_cols <<= 1;
+    const uint32_t stage = kATileBytes + (uint32_t)p.BN * BK * 2;
+    p.stages = (int)(kRingBudget / stage);
+    p.stages = p.stages < 2 ? 2 : (p.stages > kMaxStages ? kMaxStages : p.stages);
+    p.smem = smem_bytes(p.BN, p.stages);
+    p.m_tiles = (M + BM - 1) / BM;
+    const int nkb = (H + BK - 1) / BK;
+    const uint32_t ring = (uint32_t)p.stages * stage;
+    // Double the split while the tiles times the splits still fit in one wave, each split
+    // keeps enough K blocks to run its pipeline, and each slice stays a multiple of 16 wide.
+    while (2 * p.ks <= kMaxSplit && (long long)p.m_tiles * p.n_tiles * 2 * p.ks <= dev.sm_count &&
+           nkb >= 2 * p.ks * kMinKbPerSplit && p.BN % (2 * p.ks * 16) == 0 &&
+           recv_bytes(p.BN, 2 * p.ks) <= ring && cluster_fits(dev.device, 2 * p.ks, p.smem))
+        p.ks *= 2;
+    return p;
 }
 
 }  // namespace
 
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank, uint16_t* h_out,
-                              uint32_t* status_word, cudaStream_t stream) {
-    const int BN = rank >= 128 ? 128 : ((rank + 15) / 16) * 16;
-    const uint32_t tmem_cols = BN <= 32 ? 32u : (BN <= 64 ? 64u : 128u);
-    CUtensorMap map_a, map_b;
-    if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
-        !encode_2d(&map_b, w_proj, (uint64_t)rank, (uint64_t)H, (uint32_t)BN))
-        return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes(BN);
-    // Allow the largest layout (BN = 128) once per device; smaller tiles fit under it.
+                              uint32_t* status_word, cudaStream_t stream, bool beside_topk) {
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    // Allow the largest layout once per device, for both builds; every plan fits under it.
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
-    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev.device], [&] {
-        attr_err[dev.device] = cudaFuncSetAttribute(
-            projection_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(128));
+        const int smem = (int)max_smem_bytes();
+        cudaError_t e = cudaFuncSetAttribute(projection_kernel<16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(projection_kernel<1>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err[dev.device] = e;
     });
     if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
-    dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((rank + BN - 1) / BN));
-    projection_kernel<<<grid, kThreads, smem, stream>>>(map_a, map_b, h_out, M, rank, H, BN,
-                                                        tmem_cols, status_word);
-    return cudaGetLastError();
+    const ProjPlan plan = projection_plan(dev, M, H, rank);
+    CUtensorMap map_a, map_b;
+    if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
+        !encode_2d(&map_b, w_proj, (uint64_t)rank, (uint64_t)H, (uint32_t)plan.BN))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(plan.m_tiles * plan.ks), (unsigned)plan.n_tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (beside_topk)
+        return cudaLaunchKernelEx(&cfg, projection_kernel<16>, map_a, map_b, h_out, M, rank, H,
+                                  plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word);
+    return cudaLaunchKernelEx(&cfg, projection_kernel<1>, map_a, map_b, h_out, M, rank, H, plan.BN,
+                              plan.tmem_cols, plan.ks, plan.stages, status_word);
 }
 
 }  // namespace dflash
