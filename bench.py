@@ -37,7 +37,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -55,7 +54,7 @@ from draft_candidate_selector_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "selector edge scores/s (R*S*K^2)"
 UNIT = "edge_scores/s"
-PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_gemma_large.md")
+PROFILE_TOPK = os.path.join(ROOT, "profiles", "topk_gemma_large.json")
 TOPK_SOURCE = os.path.join(ROOT, "draft_candidate_selector_gb300", "csrc", "topk.cu")
 
 
@@ -94,20 +93,19 @@ def measured_peaks() -> dict:
 
 
 def profiled_traffic(workload: wl.Workload) -> float | None:
-    """DRAM bytes per top-k launch from the committed ncu summary, if it was taken on the
-    current top-k source (its sha256 is recorded with it) and on this workload."""
-    if workload.name != "gemma_large" or workload.R != 512 or not os.path.exists(PROFILE_TOPK):
+    """DRAM bytes per top-k launch at this workload's full size, from the committed ncu
+    summary profiles/topk_gemma_large.json, if that was taken on the current top-k source
+    (its sha256 is recorded with it) and on this workload; otherwise None."""
+    if not os.path.exists(PROFILE_TOPK):
         return None
     with open(PROFILE_TOPK) as f:
-        text = f.read()
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_sha and m_b):
+        prof = json.load(f)
+    if prof.get("workload") != workload.name or prof.get("R") != workload.R:
         return None
     with open(TOPK_SOURCE, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != m_sha.group(1):
+        if hashlib.sha256(f.read()).hexdigest() != prof.get("source_sha256"):
             return None
-    return float(m_b.group(1))
+    return float(prof["traffic_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -225,9 +223,10 @@ def l2_bytes(dev) -> int:
 def timed_calls(fn, steps: int, stream, flush: torch.Tensor | None) -> float:
     """Mean ms of one call of fn over `steps` calls, timed with CUDA events on `stream`.
 
-    With a flush buffer (larger than L2), the buffer is rewritten before every call and each
-    call is timed alone, so no call finds its inputs in L2; otherwise the calls run back to
-    back between two events.
+    With a flush buffer (larger than L2), the buffer is read before every call and each call
+    is timed alone, so no call finds its inputs in L2 (reading, not writing, so that the timed
+    call does not pay for writing dirty lines back); otherwise the calls run back to back
+    between two events.
     """
     if flush is None:
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -239,7 +238,7 @@ def timed_calls(fn, steps: int, stream, flush: torch.Tensor | None) -> float:
         return a.elapsed_time(b) / steps
     pairs = []
     for _ in range(steps):
-        flush.zero_()
+        flush.sum()        # a read: leaves L2 holding clean lines of the flush buffer
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -283,7 +282,7 @@ def measure_workload(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, s
     total = sum(b.values())
     topk_bytes = b["logits"] + b["ids_unary_out"]
     # Inputs within a few times the L2 would be partly served from it: flush between steps.
-    flush = (torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
+    flush = (torch.zeros(2 * l2_bytes(dev) // 4, dtype=torch.float32, device=dev)
              if total < 3 * l2_bytes(dev) else None)
     for _ in range(warmup):
         step()
@@ -295,7 +294,7 @@ def measure_workload(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, s
     out = {"R": w.R, "S": w.S, "K": w.K, "V": w.V, "H": w.H, "rank": w.rank,
            "steps": steps, "ms_per_step": ms,
            "value": w.edges_per_call / (ms / 1e3), "unit": UNIT,
-           "l2": ("L2 flushed before every step (a buffer of twice the L2 rewritten), each "
+           "l2": ("L2 flushed before every step (a buffer of twice the L2 read), each "
                   "step timed alone" if flush is not None else "inputs larger than L2"),
            "launch_mode": "eager",
            "stages_ms": {"projection": statistics.mean(s[0] for s in stages), "topk": topk_ms,
@@ -318,7 +317,7 @@ def measure_forward(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, pe
                     unary, hidden, anchors, w_proj, pred_cb, succ_cb, h, edges) -> dict:
     """The selector's forward pass on given candidates (projection, then edges), and each of
     its two kernels alone, with L2 flushed before every call."""
-    flush = torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
+    flush = torch.zeros(2 * l2_bytes(dev) // 4, dtype=torch.float32, device=dev)
     calls = {
         "forward": lambda: ds.dflash_selector_forward(cand, unary, hidden, anchors, w_proj,
                                                       pred_cb, succ_cb, h, edges),
@@ -344,7 +343,7 @@ def measure_forward(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, pe
         "frac": bound_ms / out["projection_ms"],
         "what": "max(bytes / HBM peak, FLOPs / bf16 burst peak), both measured, over the "
                 "projection's time"}
-    out["l2"] = "L2 flushed before every call (a buffer of twice the L2 rewritten)"
+    out["l2"] = "L2 flushed before every call (a buffer of twice the L2 read)"
     del flush
     return out
 
@@ -502,6 +501,28 @@ def run_ours(args, w: wl.Workload) -> None:
         stream.wait_stream(copy_out)
         copy_in.wait_stream(stream)     # the next step's copies wait for this step's kernels
 
+    def link_rate() -> float:
+        """GB/s of the host link alone: the same chunked host-to-device copies as one e2e
+        step, on the copy stream with nothing else running. One untimed pass wakes the link;
+        three passes back to back are then timed together."""
+        def copies():
+            with torch.cuda.stream(copy_in):
+                for c in range(nch):
+                    r0, r1 = bounds[c], bounds[c + 1]
+                    logits[r0:r1].copy_(logits_host[r0:r1], non_blocking=True)
+                    hidden[r0:r1].copy_(hidden_host[r0:r1], non_blocking=True)
+                    anchors[r0:r1].copy_(anchors_host[r0:r1], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        copies()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(copy_in)
+        for _ in range(3):
+            copies()
+        l1.record(copy_in)
+        torch.cuda.synchronize(dev)
+        return 3 * h2d / (l0.elapsed_time(l1) / 1e3) / 1e9
+
+    link_before = link_rate()
     e2e_step()
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -513,23 +534,9 @@ def run_ours(args, w: wl.Workload) -> None:
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1) / args.e2e_steps, w.edges_per_call, world)
-
-    # The host link's own rate, the bound of the e2e number: the same chunked host-to-device
-    # copies as one e2e step, alone on the copy stream with nothing else running, best of two.
-    link_ms = []
-    for _ in range(2):
-        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        l0.record(copy_in)
-        with torch.cuda.stream(copy_in):
-            for c in range(nch):
-                r0, r1 = bounds[c], bounds[c + 1]
-                logits[r0:r1].copy_(logits_host[r0:r1], non_blocking=True)
-                hidden[r0:r1].copy_(hidden_host[r0:r1], non_blocking=True)
-                anchors[r0:r1].copy_(anchors_host[r0:r1], non_blocking=True)
-        l1.record(copy_in)
-        torch.cuda.synchronize(dev)
-        link_ms.append(l0.elapsed_time(l1))
-    link_gbs = h2d / (min(link_ms) / 1e3) / 1e9
+    # The bound of the e2e number: the faster of two measurements of the link, taken just
+    # before and just after the e2e loop.
+    link_gbs = max(link_before, link_rate())
 
     if rank == 0:
         topk_ms = statistics.mean(s[1] for s in stages)

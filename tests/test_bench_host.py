@@ -65,8 +65,20 @@ def test_reference_arm_json_line():
 
 
 def test_profiled_traffic_requires_matching_source(tmp_path, monkeypatch):
-    prof = tmp_path / "p.md"
-    prof.write_text("source_sha256: " + "0" * 64 + "\ntraffic_bytes_per_launch: 123\n")
-    monkeypatch.setattr(bench, "PROFILE_TOPK", str(prof))
+    """The traffic figure is used only if the profile names this workload and size and was
+    taken on the top-k source as it is now."""
+    import hashlib
+    with open(bench.TOPK_SOURCE, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
     w = bench.wl.WORKLOADS["gemma_large"]
+    prof = tmp_path / "p.json"
+    monkeypatch.setattr(bench, "PROFILE_TOPK", str(prof))
+    good = {"workload": "gemma_large", "R": 512, "source_sha256": sha,
+            "traffic_bytes_per_launch": 123.0}
+    prof.write_text(json.dumps(good))
+    assert bench.profiled_traffic(w) == 123.0
+    prof.write_text(json.dumps(dict(good, source_sha256="0" * 64)))
     assert bench.profiled_traffic(w) is None          # the top-k source has changed since
+    prof.write_text(json.dumps(dict(good, R=32)))
+    assert bench.profiled_traffic(w) is None          # another size
+    assert bench.profiled_traffic(bench.wl.WORKLOADS["qwen_zipf"]) is None
