@@ -471,35 +471,51 @@ def run_ours(args, w: wl.Workload) -> None:
 
     # End to end, pipelined by chunks of requests (they are independent): the inputs of
     # chunk c+1 copy in on one stream while the selector runs on chunk c, and outputs copy
-    # out on a third stream. The host link, not the kernels, bounds this number.
+    # out on a third stream. Device buffers alternate between two sets by step, so the next
+    # step's copies overlap this step's kernels; per-chunk events keep a set's chunk from
+    # being overwritten before the kernel that reads it, or its outputs before they are read
+    # back. The host link, not the kernels, bounds this number.
     nch = max(1, min(args.e2e_chunks, w.R))
     bounds = [w.R * c // nch // 4 * 4 for c in range(nch)] + [w.R]   # 16-byte aligned chunks
     copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(nch)]
-    ev_done = [torch.cuda.Event() for _ in range(nch)]
+    sets = [dict(logits=logits, hidden=hidden, anchors=anchors, cand=cand, unary=unary, h=h,
+                 edges=edges)]
+    sets.append({k: torch.empty_like(v) for k, v in sets[0].items()})
+    ev_in = [[torch.cuda.Event() for _ in range(nch)] for _ in range(2)]
+    ev_kernel = [[torch.cuda.Event() for _ in range(nch)] for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(nch)] for _ in range(2)]
+    recorded = [False, False]
+    step_no = [0]
 
     def e2e_step():
+        p = step_no[0] % 2
+        d = sets[p]
         for c in range(nch):
             r0, r1 = bounds[c], bounds[c + 1]
             if r1 <= r0:
                 continue
             with torch.cuda.stream(copy_in):
-                logits[r0:r1].copy_(logits_host[r0:r1], non_blocking=True)
-                hidden[r0:r1].copy_(hidden_host[r0:r1], non_blocking=True)
-                anchors[r0:r1].copy_(anchors_host[r0:r1], non_blocking=True)
-                ev_in[c].record(copy_in)
-            stream.wait_event(ev_in[c])
-            ds.dflash_selector(logits[r0:r1], hidden[r0:r1], w_proj, pred_cb, succ_cb,
-                               anchors[r0:r1], w.K, cand[r0:r1], unary[r0:r1], h[r0:r1],
-                               edges[r0:r1], ws)
-            ev_done[c].record(stream)
+                if recorded[p]:
+                    copy_in.wait_event(ev_kernel[p][c])      # the set's last reader is done
+                d["logits"][r0:r1].copy_(logits_host[r0:r1], non_blocking=True)
+                d["hidden"][r0:r1].copy_(hidden_host[r0:r1], non_blocking=True)
+                d["anchors"][r0:r1].copy_(anchors_host[r0:r1], non_blocking=True)
+                ev_in[p][c].record(copy_in)
+            stream.wait_event(ev_in[p][c])
+            if recorded[p]:
+                stream.wait_event(ev_out[p][c])              # its outputs were read back
+            ds.dflash_selector(d["logits"][r0:r1], d["hidden"][r0:r1], w_proj, pred_cb, succ_cb,
+                               d["anchors"][r0:r1], w.K, d["cand"][r0:r1], d["unary"][r0:r1],
+                               d["h"][r0:r1], d["edges"][r0:r1], ws)
+            ev_kernel[p][c].record(stream)
             with torch.cuda.stream(copy_out):
-                copy_out.wait_event(ev_done[c])
-                out_edges[r0:r1].copy_(edges[r0:r1], non_blocking=True)
-                out_cand[r0:r1].copy_(cand[r0:r1], non_blocking=True)
-                out_unary[r0:r1].copy_(unary[r0:r1], non_blocking=True)
-        stream.wait_stream(copy_out)
-        copy_in.wait_stream(stream)     # the next step's copies wait for this step's kernels
+                copy_out.wait_event(ev_kernel[p][c])
+                out_edges[r0:r1].copy_(d["edges"][r0:r1], non_blocking=True)
+                out_cand[r0:r1].copy_(d["cand"][r0:r1], non_blocking=True)
+                out_unary[r0:r1].copy_(d["unary"][r0:r1], non_blocking=True)
+                ev_out[p][c].record(copy_out)
+        recorded[p] = True
+        step_no[0] += 1
 
     def link_rate() -> float:
         """GB/s of the host link alone: the same chunked host-to-device copies as one e2e
@@ -524,6 +540,7 @@ def run_ours(args, w: wl.Workload) -> None:
 
     link_before = link_rate()
     e2e_step()
+    e2e_step()
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
@@ -531,6 +548,7 @@ def run_ours(args, w: wl.Workload) -> None:
     e0.record(stream)
     for _ in range(args.e2e_steps):
         e2e_step()
+    stream.wait_stream(copy_out)                 # the last step's outputs are on the host
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1) / args.e2e_steps, w.edges_per_call, world)
@@ -570,7 +588,7 @@ def run_ours(args, w: wl.Workload) -> None:
             "launch_mode": "cuda_graph_replay" if graph is not None else "eager",
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "pipeline_chunks": nch,
+                    "pipeline_chunks": nch, "device_buffer_sets": 2,
                     "h2d_gbs_effective": h2d / (e2e_ms / 1e3) / 1e9,
                     "link_h2d_gbs_measured": link_gbs,
                     "link_frac": h2d / (e2e_ms / 1e3) / 1e9 / link_gbs},
@@ -589,7 +607,7 @@ def run_ours(args, w: wl.Workload) -> None:
             # The other workloads through the same call: their own step times, HBM fractions
             # and the oracle over each of them in full. Not part of the timed region above.
             del logits, hidden, anchors, w_proj, pred_cb, succ_cb, cand, unary, h, edges, ws
-            del logits_host, hidden_host, anchors_host, inp
+            del logits_host, hidden_host, anchors_host, inp, sets
             torch.cuda.empty_cache()
             line["per_workload"] = {
                 name: measure_workload(ds, wl.WORKLOADS[name], dev, stream, args.steps,
@@ -599,6 +617,43 @@ def run_ours(args, w: wl.Workload) -> None:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_forward(args, w: wl.Workload) -> None:
+    """The selector's forward pass alone (projection, then edges; the pages'
+    DFlash2BeamCandidateSelector.forward) on the workload's shapes, one GPU, no logits.
+
+    Inputs: the workload's seeded hidden states, projection weight, codebooks and anchors,
+    and seeded candidates (uniform ids, N(0, 1) unary values) standing in for the top-k's.
+    L2 is flushed (by a read) before every call. About 0.4 GB on the device at gemma_large,
+    so this is also the small case for full ncu captures of the projection and edges kernels.
+    """
+    import draft_candidate_selector_gb300 as ds
+    dev = torch.device("cuda", dist_env()[2])
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hidden = wl._bf16_normal(0, wl._TAG_HIDDEN, (w.R, w.S, w.H), 1.0).to(dev)
+    w_proj = wl._bf16_normal(0, wl._TAG_W, (w.rank, w.H), 1.0 / w.H ** 0.5).to(dev)
+    pred_cb = wl._bf16_normal(0, wl._TAG_PRED, (w.V, w.rank), 1.0 / w.rank ** 0.5).to(dev)
+    succ_cb = wl._bf16_normal(0, wl._TAG_SUCC, (w.V, w.rank), 1.0 / w.rank ** 0.5).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    anchors = torch.randint(0, w.V, (w.R,), generator=g, device=dev, dtype=torch.int32)
+    cand = torch.randint(0, w.V, (w.R, w.S, w.K), generator=g, device=dev, dtype=torch.int32)
+    unary = torch.randn((w.R, w.S, w.K), generator=g, device=dev)
+    h = torch.empty((w.R, w.S, w.rank), dtype=torch.bfloat16, device=dev)
+    edges = torch.empty((w.R, w.S, w.K, w.K), dtype=torch.float32, device=dev)
+    with ClockSampler(dev) as clocks:
+        f = measure_forward(ds, w, dev, stream, args.steps, args.warmup, measured_peaks(), cand,
+                            unary, hidden, anchors, w_proj, pred_cb, succ_cb, h, edges)
+    print(json.dumps({
+        "metric": "selector forward edge scores/s (R*S*K^2, given candidates)",
+        "value": f["edge_scores_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": f["forward_ms"], "higher_is_better": True,
+        "dtype": "bf16 x bf16 -> f32", "data": "synthetic (seeded)", "config": base_config(w, 1),
+        "forward": f, "gpu_launches": 2 * args.steps,
+        "device_status": ds.dflash_device_status(clear=True), "clocks": clocks.summary(),
+    }), flush=True)
 
 
 def run_lmhead(args, w: wl.Workload) -> None:
@@ -800,6 +855,9 @@ def main(argv=None) -> None:
     ap.add_argument("--sustained", type=float, default=0.0,
                     help="with --lmhead: also run the fused kernel and the cuBLAS GEMM back to "
                          "back for this many seconds each, sampling clocks and power")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the selector's forward pass alone (projection, then edges) on "
+                         "given candidates, without logits")
     ap.add_argument("--best-path", action="store_true",
                     help="time the best path through edge scores of the workload's shape instead")
     ap.add_argument("--path-steps", type=int, default=None,
@@ -821,6 +879,8 @@ def main(argv=None) -> None:
         run_lmhead(args, w)
     elif args.best_path:
         run_best_path(args, w)
+    elif args.forward:
+        run_forward(args, w)
     else:
         run_ours(args, w)
 
