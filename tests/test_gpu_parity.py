@@ -140,6 +140,28 @@ def test_topk_large_full(dev, name):
     _status_clean()
 
 
+@pytest.mark.parametrize("R,S,V,K", [
+    (3000, 1, 25003, 32),     # many rows per warp span; spans end mid-row at odd places
+    (4, 1, 20000003, 8),      # each row spread over hundreds of warps
+])
+def test_topk_large_odd_shapes(dev, R, S, V, K):
+    """Problems above 256 MB with odd shapes: thousands of short rows (V = 25003, many rows per
+    warp and spans ending mid-row at odd places), and a few rows of 20 million logits, each
+    spread over hundreds of warps whose partial lists the last to finish merges. Every row
+    against the oracle, plus the rank check on the device."""
+    rng = np.random.default_rng(R + V)
+    x = (rng.standard_normal((R, S, V), dtype=np.float32) * 5).astype(np.float32)
+    x.reshape(-1)[rng.choice(x.size, 1000, replace=False)] = 12.0     # ties near the top
+    assert x.nbytes >= 256 << 20
+    xt = torch.from_numpy(x).to(dev)
+    ids, un = ds.dflash_topk_candidates(xt, K)
+    ref_ids, ref_un = oracle.topk(x, K)
+    P.assert_ids_equal(ids.cpu().numpy(), ref_ids, f"R={R} V={V} ids")
+    P.assert_close(un.cpu().numpy(), ref_un, f"R={R} V={V} unary")
+    assert_rank_of_kth(xt, ids, K, f"R={R} V={V} rank of the K-th candidate")
+    _status_clean()
+
+
 def _topk_case(dev, x: np.ndarray, K: int, what: str):
     xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dev)
     ids, un = ds.dflash_topk_candidates(xt, K)
