@@ -291,12 +291,29 @@ def measure_workload(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, s
     ms = timed_calls(step, steps, stream, flush)
     stages = ds.dflash_trace_end(steps)
     topk_ms = statistics.mean(s[1] for s in stages)
+    # The same step captured once in a CUDA graph and replayed: for the small workloads the
+    # eager time is mostly host launch cost.
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    graph_ms = timed_calls(graph.replay, steps, stream, flush)
+    del graph
     out = {"R": w.R, "S": w.S, "K": w.K, "V": w.V, "H": w.H, "rank": w.rank,
            "steps": steps, "ms_per_step": ms,
            "value": w.edges_per_call / (ms / 1e3), "unit": UNIT,
            "l2": ("L2 flushed before every step (a buffer of twice the L2 read), each "
                   "step timed alone" if flush is not None else "inputs larger than L2"),
            "launch_mode": "eager",
+           "graph_replay": {"ms_per_step": graph_ms, "value": w.edges_per_call / (graph_ms / 1e3),
+                            "fused_hbm_frac": total / (graph_ms / 1e3) / 1e9 / peak_gbs},
            "stages_ms": {"projection": statistics.mean(s[0] for s in stages), "topk": topk_ms,
                          "edges": statistics.mean(s[2] for s in stages)},
            "topk_hbm": {"algorithmic_bytes": topk_bytes,

@@ -481,8 +481,10 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    // The edges start their gathers while the projection finishes and wait for it only to
+    // read h (programmatic dependent launch).
     e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
-                             rank, edges, status, st);
+                             rank, edges, status, st, /*after_h_producer=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "edges launch");
     return ok();
 }

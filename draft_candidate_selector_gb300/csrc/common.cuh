@@ -67,10 +67,14 @@ cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
 
 // ---------------------------------------------------------------- edges (edges.cu)
 
+// after_h_producer: h is written by the kernel launched just before on `stream`, and the ids,
+// unary values and anchors are ready. The edges are then launched as that kernel's
+// programmatic dependent (their gathers overlap its end; they wait for it before reading h).
 cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
                          const uint16_t* succ_cb, const int32_t* cand_ids, const float* unary,
                          const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
-                         int rank, float* edges, uint32_t* status_word, cudaStream_t stream);
+                         int rank, float* edges, uint32_t* status_word, cudaStream_t stream,
+                         bool after_h_producer = false);
 
 // ---------------------------------------------------------------- LM head + top-k (lmhead.cu)
 

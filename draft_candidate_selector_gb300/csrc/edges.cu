@@ -21,6 +21,9 @@
 //      Both halves are multiplied (two MMAs), so each product is exact and the sums run
 //      in fp32. B fragments (successor rows) come from ldmatrix.
 //   3. Epilogue: add unary[c], store rows q < K, columns c < K.
+// In the forward pass (projection, then edges on one stream) the edges are launched as the
+// projection's programmatic dependent: their CTAs start on free SMs, issue the id loads and
+// codebook gathers, and wait (griddepcontrol.wait) for the projection only before copying h.
 // Ids are checked against [0, V) before any copy. A bad id is never dereferenced: its
 // smem row is zeroed, its row or column of E is NaN, and the status word records
 // kStatusBadId. No thread waits on another CTA.
@@ -152,6 +155,10 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
             if (kpad != rank && lane == 0)
                 *reinterpret_cast<uint4*>(smem + dst_row + 2 * rank) = make_uint4(0, 0, 0, 0);
         }
+        // h may come from the grid launched just before this one (the forward pass launches
+        // the edges as its programmatic dependent): the gathers above need only ids, so they
+        // are already in flight. The wait returns at once when there is no such grid.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (warp == 0) {
             if (lane < chunks) cp_async16(sbase + L.h + lane * 16, h + row * rank + lane * 8);
             if (kpad != rank && lane == 0)
@@ -231,7 +238,8 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
 cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
                          const uint16_t* succ_cb, const int32_t* cand_ids, const float* unary,
                          const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
-                         int rank, float* edges, uint32_t* status_word, cudaStream_t stream) {
+                         int rank, float* edges, uint32_t* status_word, cudaStream_t stream,
+                         bool after_h_producer) {
     // Allow the largest layout (rank = 256) once per device; smaller ranks fit under it.
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -243,9 +251,18 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
     });
     if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
     const long long rows = (long long)R * S;
-    edges_kernel<<<(unsigned)rows, kThreads, edge_smem_layout(rank).total, stream>>>(
-        pred_cb, succ_cb, cand_ids, unary, h, anchors, S, K, V, rank, edges, status_word);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = edge_smem_layout(rank).total;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_h_producer ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, edges_kernel, pred_cb, succ_cb, cand_ids, unary, h, anchors,
+                              S, K, V, rank, edges, status_word);
 }
 
 }  // namespace dflash

@@ -87,6 +87,9 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     uint64_t* accum = bars + 2 * stages;    // all MMAs done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
 
+    // A dependent grid launched with programmatic serialization (the edges of the forward
+    // pass) may start now; it waits for this grid to finish before it reads h.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = ks > 1 ? (int)cluster_ctarank() : 0;
