@@ -45,27 +45,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 __device__ uint32_t g_device_status;
 
 constexpr int kMaxDevices = 64;
-// Caller streams per device that get a side stream of their own in the fused selector.
-constexpr int kMaxSideStreams = 64;
-
-// The fused selector runs the projection on a side stream beside the top-k. Each caller
-// stream has its own, so a stream being captured into a graph never shares its side stream
-// (which joins the capture) with another caller's eager work.
-struct SideStream {
-    cudaStream_t caller = nullptr;
-    std::mutex mu;   // keeps the record/wait pairs of concurrent callers from interleaving
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr;
-    cudaEvent_t join = nullptr;
-};
-
 struct DeviceSlot {
     dflash::DeviceInfo info;
     uint32_t* status_word = nullptr;
     bool ready = false;
-    std::mutex side_mu;   // guards n_side and the caller keys
-    int n_side = 0;
-    SideStream side[kMaxSideStreams];
 };
 
 std::mutex g_dev_mu;
@@ -103,37 +86,6 @@ dflash_status current_device(dflash::DeviceInfo* info, uint32_t** status_word) {
     }
     if (info) *info = s.info;
     if (status_word) *status_word = s.status_word;
-    return DFLASH_OK;
-}
-
-// The side stream and fork/join events of a caller stream on the current device, created on
-// the first fused call from that stream. *out is nullptr once kMaxSideStreams caller streams
-// have one: the projection then runs on the caller's stream, before the top-k.
-dflash_status side_stream(int device, cudaStream_t caller, SideStream** out) {
-    DeviceSlot& d = g_dev[device];
-    std::lock_guard<std::mutex> lock(d.side_mu);
-    *out = nullptr;
-    for (int i = 0; i < d.n_side; ++i)
-        if (d.side[i].caller == caller) {
-            *out = &d.side[i];
-            return DFLASH_OK;
-        }
-    if (d.n_side == kMaxSideStreams) return DFLASH_OK;
-    SideStream& s = d.side[d.n_side];
-    cudaError_t e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-        if (s.join) cudaEventDestroy(s.join);
-        if (s.fork) cudaEventDestroy(s.fork);
-        if (s.side) cudaStreamDestroy(s.side);
-        s.side = nullptr;
-        s.fork = s.join = nullptr;
-        return cuda_fail(e, "creating the selector's side stream");
-    }
-    s.caller = caller;
-    ++d.n_side;
-    *out = &s;
     return DFLASH_OK;
 }
 
@@ -266,7 +218,13 @@ size_t dflash_topk_workspace_bytes(int R, int S, int V, int K) {
 }
 
 size_t dflash_selector_workspace_bytes(int R, int S, int V, int K) {
-    return dflash_topk_workspace_bytes(R, S, V, K);
+    if (check_dims_topk(R, S, V, K) != DFLASH_OK) return 0;
+    dflash::DeviceInfo dev;
+    if (current_device(&dev, nullptr) != DFLASH_OK) return 0;
+    const long long rows = (long long)R * S;
+    // The top-k's workspace with the edge tiles' ready queue between its counters and its
+    // partial lists (zeroed together).
+    return dflash::topk_plan(dev, rows, V).workspace_bytes() + dflash::edge_queue_bytes(rows);
 }
 
 dflash_status dflash_topk_candidates(const float* logits, int R, int S, int V, int K,
@@ -418,40 +376,44 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     dflash::DeviceInfo dev;
     uint32_t* status = nullptr;
     DFLASH_TRY(current_device(&dev, &status));
-    const dflash::TopkPlan plan = dflash::topk_plan(dev, (long long)R * S, V);
-    if (workspace_bytes < plan.workspace_bytes())
+    const long long rows = (long long)R * S;
+    const dflash::TopkPlan plan = dflash::topk_plan(dev, rows, V);
+    const size_t qbytes = dflash::edge_queue_bytes(rows);
+    if (workspace_bytes < plan.workspace_bytes() + qbytes)
         return fail(DFLASH_WORKSPACE_TOO_SMALL, "workspace of %zu bytes; %zu needed",
-                    workspace_bytes, plan.workspace_bytes());
+                    workspace_bytes, plan.workspace_bytes() + qbytes);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    SideStream* side = nullptr;
-    DFLASH_TRY(side_stream(dev.device, st, &side));
     cudaEvent_t* ev = trace_slot(dev.device);
-    // The projection does not depend on the top-k, and one projection CTA per SM fits
-    // beside the top-k's: fork it onto the caller stream's side stream, join before the
-    // edges. Without a side stream it runs first on the caller's stream.
-    std::unique_lock<std::mutex> lock;
-    if (side) lock = std::unique_lock<std::mutex>(side->mu);
-    const cudaStream_t proj_st = side ? side->side : st;
+    // Workspace: the top-k's arrival counters, the edge tiles' ready queue, the top-k's partial
+    // lists. The counters and the queue are zeroed first.
+    dflash::EdgeQueue queue =
+        dflash::edge_queue_at(static_cast<char*>(workspace) + plan.counter_bytes, rows, S);
+    queue.proj_ctas = dflash::projection_ctas(dev, R * S, H, rank);
+    // Schedule, one stream. Each kernel is the next one's programmatic dependent: it may start
+    // once every CTA of the kernel before it has started, and takes only the resources that
+    // kernel leaves. So the top-k runs beside the projection (one projection CTA per SM fits
+    // beside three top-k CTAs), and the edges take the SMs that top-k CTAs leave as they
+    // finish, each scoring a tile once the ready queue hands it over (its rows are written)
+    // and the projection's count of finished CTAs is complete: most edges run in the top-k's
+    // tail. No kernel waits for one that may not have started, so nothing can stall. A traced
+    // call (dflash_trace_begin) records events between the kernels, which then run one after
+    // another, so that each can be timed.
+    const bool chain = ev == nullptr;
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    if (side) {
-        if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess) return cuda_fail(e, "fork event");
-        if ((e = cudaStreamWaitEvent(side->side, side->fork, 0)) != cudaSuccess)
-            return cuda_fail(e, "fork wait");
-    }
-    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, proj_st,
-                                  /*beside_topk=*/side != nullptr);
+    if ((e = cudaMemsetAsync(workspace, 0, plan.counter_bytes + qbytes, st)) != cudaSuccess)
+        return cuda_fail(e, "clearing the workspace");
+    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st,
+                                  /*beside_topk=*/true, queue.proj_done);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    if (ev && (e = cudaEventRecord(ev[1], proj_st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    if (side && (e = cudaEventRecord(side->join, side->side)) != cudaSuccess)
-        return cuda_fail(e, "join event");
-    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale);
+    if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "trace event");
+    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale,
+                            qbytes, /*clear_counters=*/false, queue, /*programmatic=*/chain);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    if (side && (e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess)
-        return cuda_fail(e, "join wait");
     e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
-                             rank, edges, status, st);
+                             rank, edges, status, st, /*after_h_producer=*/false, queue,
+                             /*programmatic=*/chain);
     if (e != cudaSuccess) return cuda_fail(e, "edges launch");
     if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return cuda_fail(e, "trace event");
     return ok();
@@ -638,9 +600,9 @@ dflash_status dflash_trace_end(float* stage_ms, int max_calls, int* n_calls) {
     for (int i = 0; i < n && st == DFLASH_OK; ++i) {
         cudaEvent_t* ev = &g_trace.events[4 * (size_t)i];
         cudaError_t e = cudaEventSynchronize(ev[3]);
-        // Events: [0] start, [1] projection done (side stream), [2] top-k done, [3] edges
-        // done. The projection and the top-k both start at [0] and run side by side.
-        const int from[3] = {0, 0, 2}, to[3] = {1, 2, 3};
+        // Events: [0] start, [1] projection done, [2] top-k done, [3] edges done; a traced
+        // call runs its kernels one after another, so each stage is the time between two.
+        const int from[3] = {0, 1, 2}, to[3] = {1, 2, 3};
         for (int k = 0; k < 3 && e == cudaSuccess; ++k) {
             float ms = 0.f;
             e = cudaEventElapsedTime(&ms, ev[from[k]], ev[to[k]]);

@@ -41,10 +41,38 @@ struct TopkPlan {
 
 TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V);
 
+// The fused selector's ready queue of edge tiles (one tile per (r, p) row), in the caller's
+// workspace and zeroed before every call. The top-k counts, per tile, the rows it has
+// written that the tile needs (rows p - 1 and p; only row 0 at p = 0) and pushes the tile
+// once they are all written; the projection counts its finished CTAs; edge CTA k waits
+// (bounded) for the tile pushed k-th and for the projection. A null `slots` means no queue.
+struct EdgeQueue {
+    uint32_t* tile_rows = nullptr;   // [rows] rows written that each tile needs
+    uint32_t* slots = nullptr;       // [rows] tile + 1 of the k-th ready tile; 0 until pushed
+    uint32_t* tail = nullptr;        // tiles pushed
+    uint32_t* proj_done = nullptr;   // projection CTAs finished
+    int S = 0;                       // steps per request
+    int proj_ctas = 0;               // projection CTAs to wait for
+};
+
+// Bytes of the queue's arrays for `rows` tiles, padded to 256 B.
+size_t edge_queue_bytes(long long rows);
+
+// The queue laid out at `base` (edge_queue_bytes(rows) bytes).
+EdgeQueue edge_queue_at(void* base, long long rows, int S);
+
 // softcap > 0 and scale != 1 apply the logits processor to the reported unary values.
+// `workspace` holds the arrival counters, then `extra_clear` more bytes that are zeroed with
+// them (the fused selector's queue), then the partial lists. With clear_counters false the
+// caller has zeroed them. A queue with non-null slots makes the kernel push edge tiles as
+// their rows are written. programmatic: launched as the programmatic dependent of the kernel
+// before it on the stream (it may start once that kernel's CTAs have all started; it reads
+// nothing that kernel writes).
 cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
                         int32_t* cand_ids, float* unary, void* workspace,
-                        cudaStream_t stream, float softcap = 0.f, float scale = 1.f);
+                        cudaStream_t stream, float softcap = 0.f, float scale = 1.f,
+                        size_t extra_clear = 0, bool clear_counters = true,
+                        const EdgeQueue& queue = EdgeQueue(), bool programmatic = false);
 
 // Size of the fixed device array that dflash_topk_candidates_noalloc uses as its workspace.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
@@ -60,21 +88,28 @@ cudaError_t topk_static_scratch(int device, void** ptr);
 // beside_topk selects the build that keeps to 32 registers per thread, so that a projection
 // CTA fits on an SM beside three top-k CTAs (the fused selector's schedule); the results of
 // the two builds are identical.
+// done_counter, if not null, is incremented by every CTA once its part of h is written and
+// visible device-wide (the fused selector's edges wait for it instead of a stream join).
+// projection_ctas gives the number of CTAs a launch has, for that count.
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank,
                               uint16_t* h_out, uint32_t* status_word, cudaStream_t stream,
-                              bool beside_topk = false);
+                              bool beside_topk = false, uint32_t* done_counter = nullptr);
+int projection_ctas(const DeviceInfo& dev, int M, int H, int rank);
 
 // ---------------------------------------------------------------- edges (edges.cu)
 
 // after_h_producer: h is written by the kernel launched just before on `stream`, and the ids,
 // unary values and anchors are ready. The edges are then launched as that kernel's
 // programmatic dependent (their gathers overlap its end; they wait for it before reading h).
+// queue (non-null slots): the edges take their tiles from the fused selector's ready queue;
+// with `programmatic` they are launched as the top-k's programmatic dependent.
 cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
                          const uint16_t* succ_cb, const int32_t* cand_ids, const float* unary,
                          const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
                          int rank, float* edges, uint32_t* status_word, cudaStream_t stream,
-                         bool after_h_producer = false);
+                         bool after_h_producer = false, const EdgeQueue& queue = EdgeQueue(),
+                         bool programmatic = false);
 
 // ---------------------------------------------------------------- LM head + top-k (lmhead.cu)
 

@@ -24,6 +24,9 @@
 // In the forward pass (projection, then edges on one stream) the edges are launched as the
 // projection's programmatic dependent: their CTAs start on free SMs, issue the id loads and
 // codebook gathers, and wait (griddepcontrol.wait) for the projection only before copying h.
+// In the fused selector they are the top-k's programmatic dependent instead: they take only
+// the SMs top-k CTAs leave as they finish, and each CTA scores the tile the ready queue hands
+// it (a tile whose rows the top-k has written), so most of the edges run in the top-k's tail.
 // Ids are checked against [0, V) before any copy. A bad id is never dereferenced: its
 // smem row is zeroed, its row or column of E is NaN, and the status word records
 // kStatusBadId. No thread waits on another CTA.
@@ -103,17 +106,67 @@ __host__ __device__ inline EdgeSmem edge_smem_layout(int rank) {
     return L;
 }
 
+// A wait in the ready queue gives up after this long; the CTA then sets kStatusTimeout and
+// writes nothing.
+constexpr unsigned long long kQueueWaitNs = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const uint32_t* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One thread: wait for the tile pushed k-th (k = this CTA's index: every tile is pushed once,
+// and the top-k that pushes them is resident before any edge CTA starts, so slot k always
+// fills) and for every projection CTA to be done, then return the tile (or -1 after a
+// timeout). Both counters are read with acquire loads, issued together; they pair with the
+// writers' fences, and the barrier after this call carries the order to the CTA's other
+// threads, so the tile's rows and h are visible to them.
+__device__ int take_ready_tile(const EdgeQueue& q, uint32_t* status) {
+    const uint32_t* slot = q.slots + blockIdx.x;
+    unsigned v = ld_acquire(slot);
+    unsigned done = ld_acquire(q.proj_done);
+    if (v != 0u && done >= (unsigned)q.proj_ctas) return (int)v - 1;
+    const unsigned long long t0 = now_ns();
+    while (v == 0u || done < (unsigned)q.proj_ctas) {
+        if (now_ns() - t0 > kQueueWaitNs) {
+            atomicOr(status, kStatusTimeout);
+            return -1;
+        }
+        __nanosleep(200);
+        if (v == 0u) v = ld_acquire(slot);
+        if (done < (unsigned)q.proj_ctas) done = ld_acquire(q.proj_done);
+    }
+    return (int)v - 1;
+}
+
 __global__ void __launch_bounds__(kThreads)
 edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ succ_cb,
              const int32_t* __restrict__ cand_ids, const float* __restrict__ unary,
              const uint16_t* __restrict__ h, const int32_t* __restrict__ anchors, int S, int K,
-             int V, int rank, float* __restrict__ edges, uint32_t* __restrict__ status) {
+             int V, int rank, float* __restrict__ edges, uint32_t* __restrict__ status,
+             const EdgeQueue q) {
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int s_tile;
     const EdgeSmem L = edge_smem_layout(rank);
     const uint32_t sbase = smem_u32(smem);
     int* bad = reinterpret_cast<int*>(smem + L.flags);   // bad_q[32], then bad_c[32]
 
-    const long long row = blockIdx.x;            // r * S + p
+    long long row = blockIdx.x;                  // r * S + p
+    if (q.slots != nullptr) {
+        // Fused selector: CTA k runs whichever tile comes k-th in the ready queue, once the
+        // projection has finished (all waits bounded).
+        if (threadIdx.x == 0) s_tile = take_ready_tile(q, status);
+        __syncthreads();
+        if (s_tile < 0) return;
+        row = s_tile;
+    }
     const int r = (int)(row / S);
     const int p = (int)(row % S);
     const int tid = threadIdx.x;
@@ -157,8 +210,9 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
         }
         // h may come from the grid launched just before this one (the forward pass launches
         // the edges as its programmatic dependent): the gathers above need only ids, so they
-        // are already in flight. The wait returns at once when there is no such grid.
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // are already in flight. The wait returns at once when there is no such grid. With the
+        // ready queue, the tile's rows and h are already known to be written.
+        if (q.slots == nullptr) asm volatile("griddepcontrol.wait;" ::: "memory");
         if (warp == 0) {
             if (lane < chunks) cp_async16(sbase + L.h + lane * 16, h + row * rank + lane * 8);
             if (kpad != rank && lane == 0)
@@ -239,7 +293,7 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
                          const uint16_t* succ_cb, const int32_t* cand_ids, const float* unary,
                          const uint16_t* h, const int32_t* anchors, int R, int S, int K, int V,
                          int rank, float* edges, uint32_t* status_word, cudaStream_t stream,
-                         bool after_h_producer) {
+                         bool after_h_producer, const EdgeQueue& queue, bool programmatic) {
     // Allow the largest layout (rank = 256) once per device; smaller ranks fit under it.
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -260,9 +314,9 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
     cfg.dynamicSmemBytes = edge_smem_layout(rank).total;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = after_h_producer ? 1 : 0;
+    cfg.numAttrs = (after_h_producer || programmatic) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, edges_kernel, pred_cb, succ_cb, cand_ids, unary, h, anchors,
-                              S, K, V, rank, edges, status_word);
+                              S, K, V, rank, edges, status_word, queue);
 }
 
 }  // namespace dflash

@@ -72,7 +72,8 @@ template <int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                   uint16_t* __restrict__ out, int M, int N, int Kdim, int BN, uint32_t tmem_cols,
-                  int ks, int stages, uint32_t* __restrict__ status) {
+                  int ks, int stages, uint32_t* __restrict__ status,
+                  uint32_t* __restrict__ done_counter) {
     extern __shared__ uint8_t smem_raw[];
     // The 128-byte swizzle pattern repeats every 1024 B: tiles start on that boundary. Every
     // CTA has the same layout, so an offset names the same place in each CTA of a cluster.
@@ -283,8 +284,12 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
             }
         }
     }
+    // This CTA's part of h is written: make it visible device-wide, then count the CTA (the
+    // fused selector's edges wait for the count rather than for the stream).
+    if (done_counter != nullptr) __threadfence();
     tc_fence_before();
     __syncthreads();
+    if (done_counter != nullptr && threadIdx.x == 0) atomicAdd(done_counter, 1u);
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -414,7 +419,8 @@ ProjPlan projection_plan(const DeviceInfo& dev, int M, int H, int rank) {
 
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank, uint16_t* h_out,
-                              uint32_t* status_word, cudaStream_t stream, bool beside_topk) {
+                              uint32_t* status_word, cudaStream_t stream, bool beside_topk,
+                              uint32_t* done_counter) {
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     // Allow the largest layout once per device, for both builds; every plan fits under it.
     static std::once_flag once[64];
@@ -448,9 +454,15 @@ cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
     cfg.numAttrs = 1;
     if (beside_topk)
         return cudaLaunchKernelEx(&cfg, projection_kernel<16>, map_a, map_b, h_out, M, rank, H,
-                                  plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word);
+                                  plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word,
+                                  done_counter);
     return cudaLaunchKernelEx(&cfg, projection_kernel<1>, map_a, map_b, h_out, M, rank, H, plan.BN,
-                              plan.tmem_cols, plan.ks, plan.stages, status_word);
+                              plan.tmem_cols, plan.ks, plan.stages, status_word, done_counter);
+}
+
+int projection_ctas(const DeviceInfo& dev, int M, int H, int rank) {
+    const ProjPlan plan = projection_plan(dev, M, H, rank);
+    return plan.m_tiles * plan.ks * plan.n_tiles;
 }
 
 }  // namespace dflash

@@ -187,6 +187,30 @@ __device__ __forceinline__ void write_row(uint64_t e, long long row, int lane, i
     }
 }
 
+// The fused selector's ready queue: tile t (row t's edge scores) is pushed once the rows it
+// needs are written.
+__device__ __forceinline__ void enqueue_tile(const EdgeQueue& q, int t) {
+    const unsigned k = atomicAdd(q.tail, 1u);
+    atomicExch(q.slots + k, (unsigned)t + 1u);
+}
+
+// Row `row` is written: count it for the two tiles that need it (tile row, which also needs
+// row - 1 unless it is a request's first step, and tile row + 1, unless row is the request's
+// last step) and push each tile whose rows are now all written. Every lane's writes of the
+// row are made visible device-wide before the counts.
+__device__ __forceinline__ void push_ready(const EdgeQueue& q, long long row, int lane) {
+    if (q.slots == nullptr) return;
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+        const int p = (int)(row % q.S);
+        if (atomicAdd(q.tile_rows + row, 1u) + 1u == (p == 0 ? 1u : 2u)) enqueue_tile(q, (int)row);
+        if (p + 1 < q.S && atomicAdd(q.tile_rows + row + 1, 1u) + 1u == 2u)
+            enqueue_tile(q, (int)row + 1);
+    }
+    __syncwarp();
+}
+
 // First group of a row segment, with the list still empty. The lane-bests, sorted, start
 // the list: they are K or more real entries, so the K-th of them is a valid threshold.
 // The group is then read again (it is in L2 by now) and its other values are offered;
@@ -298,7 +322,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 topk_kernel(const float* __restrict__ logits, long long total, long long span, int warps, int V,
             int K, float softcap, float scale, int32_t* __restrict__ cand_ids,
             float* __restrict__ unary, uint32_t* __restrict__ counters,
-            uint64_t* __restrict__ partials) {
+            uint64_t* __restrict__ partials, const EdgeQueue queue) {
+    // A grid launched as this one's programmatic dependent (the fused selector's edges) may
+    // start once every CTA of this grid has: it takes only the resources this grid frees, and
+    // it reads nothing of this grid's output until the ready queue says it is written.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (gw >= warps) return;
@@ -326,6 +354,7 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
         const int w1 = (int)((row_base + V - 1) / span);
         if (w0 == w1) {
             write_row(L.e, r, lane, K, softcap, scale, cand_ids, unary);
+            push_ready(queue, r, lane);
             continue;
         }
         // Only a warp's first and last rows can be shared: one slot for each.
@@ -347,6 +376,7 @@ topk_kernel(const float* __restrict__ logits, long long total, long long span, i
             m = merge_lists(m, other, lane);
         }
         write_row(m, r, lane, K, softcap, scale, cand_ids, unary);
+        push_ready(queue, r, lane);
     }
 }
 
@@ -419,23 +449,49 @@ TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V) {
     return p;
 }
 
+size_t edge_queue_bytes(long long rows) {
+    return (size_t)(((2 * rows + 2) * 4 + 255) / 256 * 256);
+}
+
+EdgeQueue edge_queue_at(void* base, long long rows, int S) {
+    EdgeQueue q;
+    uint32_t* w = static_cast<uint32_t*>(base);
+    q.tile_rows = w;
+    q.slots = w + rows;
+    q.tail = w + 2 * rows;
+    q.proj_done = w + 2 * rows + 1;
+    q.S = S;
+    return q;
+}
+
 cudaError_t launch_topk(const TopkPlan& plan, const float* logits, int V, int K,
                         int32_t* cand_ids, float* unary, void* workspace, cudaStream_t stream,
-                        float softcap, float scale) {
+                        float softcap, float scale, size_t extra_clear, bool clear_counters,
+                        const EdgeQueue& queue, bool programmatic) {
     uint32_t* counters = static_cast<uint32_t*>(workspace);
     uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
-                                                     plan.counter_bytes);
-    cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
-    if (err != cudaSuccess) return err;
+                                                     plan.counter_bytes + extra_clear);
+    if (clear_counters) {
+        cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes + extra_clear, stream);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)plan.blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
     if (plan.variant == 0)
-        topk_kernel<3, kUnroll><<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span,
-                                                             plan.warps, V, K, softcap, scale,
-                                                             cand_ids, unary, counters, partials);
-    else
-        topk_kernel<2, kUnroll><<<plan.blocks, kThreads, 0, stream>>>(logits, plan.total, plan.span,
-                                                             plan.warps, V, K, softcap, scale,
-                                                             cand_ids, unary, counters, partials);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, topk_kernel<3, kUnroll>, logits, plan.total, plan.span,
+                                  plan.warps, V, K, softcap, scale, cand_ids, unary, counters,
+                                  partials, queue);
+    return cudaLaunchKernelEx(&cfg, topk_kernel<2, kUnroll>, logits, plan.total, plan.span,
+                              plan.warps, V, K, softcap, scale, cand_ids, unary, counters,
+                              partials, queue);
 }
 
 }  // namespace dflash

@@ -193,16 +193,15 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
                                      dflash_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
- * The whole selector in one call, with no host round trip. Step 2 (projection) runs on a
- * library-owned side stream beside step 1 (top-k) on `stream`; step 3 (edges) follows
- * both on `stream`. Each caller stream gets a side stream of its own, on its first fused
- * call (up to 64 caller streams per device; beyond that the projection runs on `stream`
- * itself, before the top-k). The call returns once everything is enqueued; later work on
- * `stream` sees all outputs. It is safe to capture in a CUDA graph: the side stream joins
- * the capture through an event, and since it belongs to the capturing stream alone, eager
- * calls on other streams meanwhile stay out of the graph. Make one call on the device
- * before capturing. The outputs, workspace, softcap and scale are as in the three calls
- * above; the edge scores use the processed unary values.
+ * The whole selector in one call, with no host round trip. All three steps run on `stream`,
+ * each kernel launched as the programmatic dependent of the one before it: the top-k (step 1)
+ * runs beside the projection (step 2), and the edges (step 3) take the SMs the top-k leaves as
+ * it finishes, scoring each (r, p) tile as soon as the top-k has written the rows it needs.
+ * The call returns once everything is enqueued; later work on `stream` sees all outputs. It is
+ * safe to capture in a CUDA graph; make one call on the device before capturing. The
+ * workspace holds the top-k's and the edge tiles' bookkeeping (its size query includes
+ * both; its contents on entry do not matter). The outputs, softcap and scale are as in the
+ * three calls above; the edge scores use the processed unary values.
  * Source: the draft step captures the candidate head and the selector together
  * (module docstring of the page).
  * ---------------------------------------------------------------------------------- */
@@ -253,10 +252,9 @@ dflash_status dflash_selector_forward(const int32_t* cand_ids, const float* unar
  * everything is enqueued. The candidates may differ from an exact computation only where two
  * logits differ by less than their fp32 accumulation error (see dflash_lmhead_topk); the edge
  * scores are those of the candidates returned. Requires the ranges of dflash_selector and
- * H a multiple of 8. A traced call (dflash_trace_begin) records the same four events; its
- * top-k time counts from the start and so includes the projection. It can be captured in a
- * CUDA graph; make one call on the device before capturing (the first call sets the kernels'
- * shared-memory limits).
+ * H a multiple of 8. A traced call (dflash_trace_begin) records the same four events. It can
+ * be captured in a CUDA graph; make one call on the device before capturing (the first call
+ * sets the kernels' shared-memory limits).
  * ---------------------------------------------------------------------------------- */
 size_t dflash_selector_lmhead_workspace_bytes(int R, int S, int V, int K);
 
@@ -315,11 +313,12 @@ dflash_status dflash_selftest_wait_timeout(void);
  * the pages; this is a profiling aid.
  * dflash_trace_begin(n) creates 4 timing events for each of the next n selector calls
  * made from this process on the current device. Each traced call records them: at its
- * start, when the projection is done (side stream), when the top-k is done and when the
- * edges are done. dflash_trace_end waits for the events. It writes up to max_calls rows
- * of 3 stage times (ms) into `stage_ms` (a host array of 3 * max_calls floats): the
- * projection and the top-k, each from the start (they run side by side), and the edges.
- * It stores the row count in *n_calls, then releases the events.
+ * start, when the projection is done, when the top-k is done and when the edges are done,
+ * and its kernels then run one after another (untraced, dflash_selector overlaps them), so
+ * that each can be timed. dflash_trace_end waits for the events. It writes up to max_calls
+ * rows of 3 stage times (ms) into `stage_ms` (a host array of 3 * max_calls floats): the
+ * projection, the top-k and the edges, each the time between two events. It stores the row
+ * count in *n_calls, then releases the events.
  * ---------------------------------------------------------------------------------- */
 dflash_status dflash_trace_begin(int n_calls);
 dflash_status dflash_trace_end(float* stage_ms, int max_calls, int* n_calls);
