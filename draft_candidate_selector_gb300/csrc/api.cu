@@ -44,6 +44,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Bits the kernels set on problems they detect; read through dflash_device_status.
 __device__ uint32_t g_device_status;
 
+// Zeroed scratch of dflash_selftest_wait_timeout's queue check (1 KB).
+__device__ __align__(16) uint32_t g_selftest_buffer[256];
+
 constexpr int kMaxDevices = 64;
 struct DeviceSlot {
     dflash::DeviceInfo info;
@@ -551,6 +554,27 @@ dflash_status dflash_selftest_wait_timeout(void) {
     if (e != cudaSuccess) return cuda_fail(e, "wait self-check launch");
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "wait self-check");
+    // The edge tiles' ready queue: one edge CTA waits for a tile that is never pushed. Its
+    // queue and every array it is given live in a zeroed static buffer; it gives up before it
+    // reads any of them and writes nothing.
+    void* buf = nullptr;
+    e = cudaGetSymbolAddress(&buf, g_selftest_buffer);
+    if (e == cudaSuccess) e = cudaMemset(buf, 0, sizeof(g_selftest_buffer));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cuda_fail(e, "queue self-check buffer");
+    }
+    uint32_t* w = static_cast<uint32_t*>(buf);
+    dflash::EdgeQueue q = dflash::edge_queue_at(w, 1, 1);
+    q.proj_ctas = 1;
+    const uint16_t* b16 = reinterpret_cast<const uint16_t*>(w + 64);
+    e = dflash::launch_edges(dev, b16, b16, reinterpret_cast<const int32_t*>(w + 64),
+                             reinterpret_cast<const float*>(w + 64), b16,
+                             reinterpret_cast<const int32_t*>(w + 64), 1, 1, 1, 1, 8,
+                             reinterpret_cast<float*>(w + 128), status, nullptr, false, q);
+    if (e != cudaSuccess) return cuda_fail(e, "queue self-check launch");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "queue self-check");
     return ok();
 }
 

@@ -301,10 +301,11 @@ dflash_status dflash_device_status(uint32_t* flags, int clear);
 /* ------------------------------------------------------------------------------------
  * Self-check of the wait limit. There is no counterpart on the pages; this is a test aid for
  * the failure path. It launches one thread that waits on an mbarrier nothing ever arrives
- * on, through the same bounded wait the pipelined kernels use (projection, LM-head top-k).
- * The wait gives up after about one second, sets DFLASH_DEVICE_TIMEOUT in the status word,
- * and the kernel returns: nothing traps or faults, and the context stays usable. Synchronises
- * the device; read and clear the bit with dflash_device_status.
+ * on, through the same bounded wait the pipelined kernels use (projection, LM-head top-k),
+ * then one edge CTA that waits in the fused selector's ready queue for a tile nothing ever
+ * pushes. Each wait gives up after about one second, sets DFLASH_DEVICE_TIMEOUT in the status
+ * word, and the kernel returns: nothing traps or faults, nothing is written, and the context
+ * stays usable. Synchronises the device; read and clear the bit with dflash_device_status.
  * ---------------------------------------------------------------------------------- */
 dflash_status dflash_selftest_wait_timeout(void);
 

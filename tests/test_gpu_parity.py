@@ -791,8 +791,10 @@ def test_selector_lmhead(dev, R, S, K, V, H, rank, cap, scale):
 
 def test_wait_timeout_is_reported_and_the_context_survives(dev):
     """The failure path of the bounded waits, without a fault: a wait on an mbarrier that
-    nothing arrives on gives up after about a second and sets the timeout bit; afterwards the
-    same context still runs the top-k correctly."""
+    nothing arrives on, then an edge CTA's wait in the fused selector's ready queue for a tile
+    nothing pushes, each give up after about a second and set the timeout bit; afterwards the
+    same context still runs the top-k and the fused selector (ready queue included)
+    correctly."""
     import time
     lib = _native.load()
     ds.dflash_device_status(clear=True)
@@ -800,9 +802,10 @@ def test_wait_timeout_is_reported_and_the_context_survives(dev):
     _native.check(lib.dflash_selftest_wait_timeout())
     dt = time.perf_counter() - t0
     assert ds.dflash_device_status(clear=True) & _native.DEVICE_TIMEOUT
-    assert 0.5 < dt < 30.0, dt
+    assert 1.5 < dt < 60.0, dt
     x = np.random.default_rng(3).standard_normal((2, 3, 5000)).astype(np.float32)
     _topk_case(dev, x, 8, "top-k after a timeout")
+    _selector_check(dev, host_inputs("small_ties"), "fused selector after a timeout")
     _status_clean()
 
 
