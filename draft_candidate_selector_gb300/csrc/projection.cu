@@ -9,17 +9,19 @@
 // Linear [out, in]) are both K-major, which is the native operand form of tcgen05.mma.
 //
 // Tiling. The output is cut into 128 x BN tiles, BN = the rank rounded up to 16, at most
-// 128 (N tiles beyond the first re-read the same hidden-state tile, mostly from L2). A
-// cluster of `ks` CTAs computes one tile, splitting K: CTA s of the cluster (its cluster
-// rank) takes the contiguous K blocks [s * nkb / ks, (s + 1) * nkb / ks). The host doubles
-// ks, from 1, while the tiles times ks still fit the SMs in one wave and every split keeps
-// at least 8 K blocks (gemma_large: 60 x 2 tiles, ks = 1; gemma_softcap: 30 tiles, ks = 4;
-// qwen_zipf: 8 tiles, ks = 4). Each CTA's time is set by its chain of K blocks: a stage
-// makes a round trip (TMA load, MMAs, release) of about 1.7 us, with 6 stages in flight,
-// whatever the stage's bytes. In each CTA:
+// 256 (the widest N of one M = 128 tcgen05.mma). Wide tiles pay: measured on GB300, an
+// M = 128, K = 16 MMA takes about as long at N = 128 as at N = 256 (a CTA's chain of MMAs
+// with the loads taken out: 31 us for 84 K blocks at N = 128, 33 us at N = 256), so a
+// 128-wide tile does half the work per MMA. A cluster of `ks` CTAs computes one tile,
+// splitting K: CTA s of the cluster (its cluster rank) takes the contiguous K blocks
+// [s * nkb / ks, (s + 1) * nkb / ks). The host doubles ks, from 1, while the tiles times ks
+// still fit the SMs in one wave and every split keeps at least 8 K blocks (gemma_large:
+// 60 tiles of 256 columns, ks = 2; gemma_softcap: 30 tiles, ks = 4; qwen_zipf: 8 tiles,
+// ks = 4). In each CTA:
 //   * warp 0, one lane: TMA producer. Per 64-wide K block it loads a 128x64 A tile and a
-//     BNx64 B tile (128-byte swizzle) into a ring of `stages` shared-memory stages (6 at
-//     BN = 128, up to 8). Completion is tracked on mbarriers by transaction bytes.
+//     BNx64 B tile (128-byte swizzle) into a ring of `stages` shared-memory stages (192 KB:
+//     4 at BN = 256, 6 at BN = 128, up to 8). Completion is tracked on mbarriers by
+//     transaction bytes.
 //   * warp 1, one lane: MMA issuer. tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), M=128,
 //     N=BN, K=16, four per K block, accumulating in tensor memory. tcgen05.commit frees
 //     each stage and finally signals the accumulator.
@@ -29,10 +31,11 @@
 //       ks > 1: the tile's columns are cut into ks slices of BN / ks; CTA s owns slice s.
 //       Once every CTA's MMAs are done (cluster barrier), each CTA writes its fp32
 //       partials of the slices it does not own into the owners' shared memory
-//       (distributed shared memory, over the now idle ring), a second cluster barrier
-//       makes them visible, and each owner adds the ks partials of its slice in split
-//       order (0, 1, ...), rounds to bf16 and stores. The sum order is fixed, so the result
-//       does not depend on which CTA owns which slice.
+//       (distributed shared memory, over the now idle ring, in a layout where each warp
+//       store covers 512 contiguous bytes), a second cluster barrier makes them visible,
+//       and each owner adds the ks partials of its slice in split order (0, 1, ...), rounds
+//       to bf16 and stores. The sum order is fixed, so the result does not depend on which
+//       CTA owns which slice.
 // Out-of-range rows, columns and K are zero-filled by TMA and never stored.
 // Every mbarrier wait is bounded, about one second by %globaltimer. On expiry the kernel
 // sets kStatusTimeout, skips the remaining work, still takes part in both cluster
@@ -59,11 +62,17 @@ constexpr uint32_t kATileBytes = BM * BK * 2;
 constexpr uint32_t kRingBudget = 192u * 1024u;   // shared memory for the stage ring
 constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 8;
+constexpr int kMaxBN = 256;            // widest N tile: one tcgen05.mma (M = 128) takes N <= 256
 constexpr int kMinKbPerSplit = 8;      // K blocks each split must keep
 
-// Bytes of one receive row of a slice of `slice` fp32 columns, padded by 16 B so that the
-// owner's row-per-thread reads spread over the banks.
-__host__ __device__ constexpr uint32_t recv_row_bytes(int slice) { return (uint32_t)slice * 4u + 16u; }
+// Receive area of the K-split reduction. A slot holds one other CTA's fp32 partials of
+// this CTA's slice as [slice / 4][BM rows][4 columns]: thread t (row t) moves 16 bytes at
+// t * 16 within a 4-column group, so a warp's 32 stores or loads are 512 contiguous bytes
+// and touch every bank once.
+__host__ __device__ constexpr uint32_t recv_slot_bytes(int slice) { return (uint32_t)slice * BM * 4u; }
+__host__ __device__ constexpr uint32_t recv_offset(int c, int row) {
+    return (uint32_t)(c >> 2) * (BM * 16u) + (uint32_t)row * 16u;
+}
 
 // Two builds. kMinBlocks = 16 caps the registers at 32 per thread, so that one projection
 // CTA fits beside three top-k CTAs on an SM (the fused selector runs them side by side);
@@ -217,69 +226,83 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
         // partials of the j-th other CTA (in split order), one padded row per tile row.
         // Barrier 1: every CTA of the cluster is done with its ring.
         cluster_sync();
+        const int me = (int)cluster_ctarank();
+        const int slice = BN / ks;                   // a multiple of 16
         if (ready) {
-            const int me = (int)cluster_ctarank();
-            const int slice = BN / ks;               // a multiple of 16
-            const uint32_t rrow = recv_row_bytes(slice);
             for (int o = 0; o < ks; ++o) {
                 if (o == me) continue;
                 // In owner o's receive area, sender `me` uses slot me (or me - 1).
                 const uint32_t dst = mapa(smem_u32(smem) + (uint32_t)(me < o ? me : me - 1) *
-                                              (uint32_t)BM * rrow + (uint32_t)trow * rrow,
+                                              recv_slot_bytes(slice) + recv_offset(0, trow),
                                           (uint32_t)o);
-                for (int c = 0; c < slice; c += 4) {
-                    uint32_t v[4];
-                    tmem_ld_32x32b_x4(tlane + (uint32_t)(o * slice + c), v);
-                    st_cluster_v4(dst + (uint32_t)c * 4u, v[0], v[1], v[2], v[3]);
+                if constexpr (kMinBlocks == 1) {
+                    for (int c = 0; c < slice; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(tlane + (uint32_t)(o * slice + c), v);
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            st_cluster_v4(dst + recv_offset(c + j, 0), v[j], v[j + 1], v[j + 2],
+                                          v[j + 3]);
+                    }
+                } else {
+                    for (int c = 0; c < slice; c += 4) {
+                        uint32_t v[4];
+                        tmem_ld_32x32b_x4(tlane + (uint32_t)(o * slice + c), v);
+                        st_cluster_v4(dst + recv_offset(c, 0), v[0], v[1], v[2], v[3]);
+                    }
                 }
             }
         }
         // Barrier 2: the partials written to peers are visible to them.
         cluster_sync();
         if (ready) {
-            // Every lane runs the warp-wide tensor-memory loads; only rows < M are stored.
-            const int me = (int)cluster_ctarank();
-            const int slice = BN / ks;
-            const uint32_t rrow = recv_row_bytes(slice);
-            const uint8_t* rbase = smem + (size_t)trow * rrow;
-            for (int c = 0; c < slice; c += 8) {
+            // Every lane runs the warp-wide tensor-memory loads; only rows < M are stored. The
+            // sum runs in split order 0, 1, ...: acc = p0, then acc += p1, and so on, so it
+            // does not depend on which CTA owns the slice.
+            constexpr int kChunk = kMinBlocks == 1 ? 16 : 8;
+            const int row = m0 + trow;
+            for (int c = 0; c < slice; c += kChunk) {
                 const int col = me * slice + c;      // within the tile
                 if (n0 + col >= N) break;            // warp-uniform; N % 8 == 0
-                // This CTA's own partial (one load, one wait), then the sum in split order
-                // 0, 1, ...: acc = p0, then acc += p1, and so on.
-                uint32_t v[8];
-                tmem_ld_32x32b_x8(tlane + (uint32_t)col, v);
-                float acc[8];
+                uint32_t v[kChunk];
+                if constexpr (kChunk == 16) tmem_ld_32x32b_x16(tlane + (uint32_t)col, v);
+                else tmem_ld_32x32b_x8(tlane + (uint32_t)col, v);
+                float acc[kChunk];
                 if (me == 0) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] = __uint_as_float(v[j]);
+                    for (int j = 0; j < kChunk; ++j) acc[j] = __uint_as_float(v[j]);
                 } else {
-                    const float4* q = reinterpret_cast<const float4*>(rbase + (size_t)c * 4);
-                    const float4 a = q[0], b = q[1];
-                    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-                    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+#pragma unroll
+                    for (int j = 0; j < kChunk; j += 4) {
+                        const float4 a = *reinterpret_cast<const float4*>(smem + recv_offset(c + j, trow));
+                        acc[j] = a.x; acc[j + 1] = a.y; acc[j + 2] = a.z; acc[j + 3] = a.w;
+                    }
                 }
                 for (int s = 1; s < ks; ++s) {
                     if (s == me) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[j] += __uint_as_float(v[j]);
+                        for (int j = 0; j < kChunk; ++j) acc[j] += __uint_as_float(v[j]);
                     } else {
-                        const float4* q = reinterpret_cast<const float4*>(
-                            rbase + (size_t)(s < me ? s : s - 1) * BM * rrow + (size_t)c * 4);
-                        const float4 a = q[0];
-                        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                        const float4 b = q[1];
-                        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+                        const uint8_t* slot = smem + (size_t)(s < me ? s : s - 1) * recv_slot_bytes(slice);
+#pragma unroll
+                        for (int j = 0; j < kChunk; j += 4) {
+                            const float4 a = *reinterpret_cast<const float4*>(slot + recv_offset(c + j, trow));
+                            acc[j] += a.x; acc[j + 1] += a.y; acc[j + 2] += a.z; acc[j + 3] += a.w;
+                        }
                     }
                 }
-                const int row = m0 + trow;
                 if (row < M) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
-                    w.y = pack_bf16x2(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
-                    w.z = pack_bf16x2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
-                    w.w = pack_bf16x2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
-                    *reinterpret_cast<uint4*>(out + (long long)row * N + n0 + col) = w;
+                    uint4* o4 = reinterpret_cast<uint4*>(out + (long long)row * N + n0 + col);
+#pragma unroll
+                    for (int j = 0; j < kChunk; j += 8) {
+                        // N % 8 == 0: each 8-column piece is all in or all out.
+                        if (n0 + col + j < N)
+                            o4[j >> 3] = make_uint4(
+                                pack_bf16x2(__float_as_uint(acc[j]), __float_as_uint(acc[j + 1])),
+                                pack_bf16x2(__float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3])),
+                                pack_bf16x2(__float_as_uint(acc[j + 4]), __float_as_uint(acc[j + 5])),
+                                pack_bf16x2(__float_as_uint(acc[j + 6]), __float_as_uint(acc[j + 7])));
+                    }
                 }
             }
         }
@@ -336,7 +359,7 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
 }
 
 struct ProjPlan {
-    int BN = 0;             // N tile: the rank rounded up to 16, at most 128
+    int BN = 0;             // N tile: the rank rounded up to 16, at most 256
     uint32_t tmem_cols = 0; // power of two >= max(32, BN)
     int stages = 0;         // ring stages
     int ks = 1;             // K splits per tile = CTAs per cluster
@@ -346,7 +369,7 @@ struct ProjPlan {
 };
 
 uint32_t recv_bytes(int BN, int ks) {
-    return ks > 1 ? (uint32_t)(ks - 1) * BM * recv_row_bytes(BN / ks) : 0u;
+    return ks > 1 ? (uint32_t)(ks - 1) * recv_slot_bytes(BN / ks) : 0u;
 }
 
 size_t smem_bytes(int BN, int stages) {
@@ -357,7 +380,7 @@ size_t smem_bytes(int BN, int stages) {
 // Largest dynamic shared memory any plan asks for (set once per device).
 size_t max_smem_bytes() {
     size_t m = 0;
-    for (int BN = 16; BN <= 128; BN += 16) {
+    for (int BN = 16; BN <= kMaxBN; BN += 16) {
         const uint32_t stage = kATileBytes + (uint32_t)BN * BK * 2;
         int st = (int)(kRingBudget / stage);
         st = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
@@ -395,7 +418,7 @@ bool cluster_fits(int device, int ks, size_t smem) {
 
 ProjPlan projection_plan(const DeviceInfo& dev, int M, int H, int rank) {
     ProjPlan p;
-    p.BN = rank >= 128 ? 128 : ((rank + 15) / 16) * 16;
+    p.BN = rank >= kMaxBN ? kMaxBN : ((rank + 15) / 16) * 16;
     p.n_tiles = (rank + p.BN - 1) / p.BN;
     p.tmem_cols = 32;
     while (p.tmem_cols < (uint32_t)p.BN) p.tmem_cols <<= 1;
