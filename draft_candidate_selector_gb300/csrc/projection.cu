@@ -77,7 +77,7 @@ __host__ __device__ constexpr uint32_t recv_offset(int c, int row) {
 // Two builds. kMinBlocks = 16 caps the registers at 32 per thread, so that one projection
 // CTA fits beside three top-k CTAs on an SM (the fused selector runs them side by side);
 // kMinBlocks = 1 leaves the compiler free, for calls where nothing runs beside it.
-template <int kMinBlocks>
+template <int kMinBlocks, bool kPair>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                   uint16_t* __restrict__ out, int M, int N, int Kdim, int BN, uint32_t tmem_cols,
@@ -88,7 +88,11 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     // CTA has the same layout, so an offset names the same place in each CTA of a cluster.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t b_tile_bytes = (uint32_t)BN * BK * 2;
+    // A CTA pair computes a 256 x BN tile: each CTA stages its own 128 rows of A and half of
+    // B's BN rows, and holds its 128 rows of the accumulator.
+    constexpr int kCta = kPair ? 2 : 1;
+    const int bn_cta = BN / kCta;                // B rows this CTA stages
+    const uint32_t b_tile_bytes = (uint32_t)bn_cta * BK * 2;
     uint8_t* sa = smem;
     uint8_t* sb = smem + stages * kATileBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sb + stages * b_tile_bytes);
@@ -102,8 +106,10 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int split = ks > 1 ? (int)cluster_ctarank() : 0;
-    const int m0 = (blockIdx.x / ks) * BM;
+    const int crank = (ks > 1 || kPair) ? (int)cluster_ctarank() : 0;
+    const int pr = kPair ? (crank & 1) : 0;      // CTA within the pair (0 issues the MMAs)
+    const int split = crank / kCta;
+    const int m0 = (blockIdx.x / (ks * kCta)) * (BM * kCta) + pr * BM;
     const int n0 = blockIdx.y * BN;
     const int nkb = (Kdim + BK - 1) / BK;
     const int kb0 = split * nkb / ks;
@@ -120,16 +126,28 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
         asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(tmem_cols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (kPair) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(tmem_cols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(tmem_cols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // A pair's loads count on the even CTA's barriers and its commits arrive on both CTAs'
+    // barriers: every barrier of the cluster is initialised before any of that starts.
+    if constexpr (kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint16_t pair_mask = (uint16_t)(3u << (crank & ~1));
 
     if (warp == 0 && lane == 0) {
         // TMA producer.
@@ -141,9 +159,18 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
                 break;
             }
             const uint32_t fb = smem_u32(&full[s]);
-            mbar_expect_tx(fb, kATileBytes + b_tile_bytes);
-            tma_load_2d(smem_u32(sa + s * kATileBytes), &map_a, fb, (kb0 + i) * BK, m0);
-            tma_load_2d(smem_u32(sb + s * b_tile_bytes), &map_b, fb, (kb0 + i) * BK, n0);
+            if constexpr (kPair) {
+                // Both CTAs' bytes count on the even CTA's barrier, which that CTA arms.
+                const uint32_t lead = mapa(fb, (uint32_t)(crank & ~1));
+                if (pr == 0) mbar_expect_tx(fb, 2u * (kATileBytes + b_tile_bytes));
+                tma_load_2d_pair(smem_u32(sa + s * kATileBytes), &map_a, lead, (kb0 + i) * BK, m0);
+                tma_load_2d_pair(smem_u32(sb + s * b_tile_bytes), &map_b, lead, (kb0 + i) * BK,
+                                 n0 + pr * bn_cta);
+            } else {
+                mbar_expect_tx(fb, kATileBytes + b_tile_bytes);
+                tma_load_2d(smem_u32(sa + s * kATileBytes), &map_a, fb, (kb0 + i) * BK, m0);
+                tma_load_2d(smem_u32(sb + s * b_tile_bytes), &map_b, fb, (kb0 + i) * BK, n0);
+            }
             issued = i + 1;
             if (++s == stages) {
                 s = 0;
@@ -153,11 +180,15 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
         // The last load into each stage must land before the CTA may leave, or its ring be
         // reused for the partial sums, also after a timeout. Each wait is bounded; in the
         // normal case those loads were consumed long ago and every wait returns at once.
-        for (int q = issued > stages ? issued - stages : 0; q < issued; ++q)
-            (void)mbar_wait(smem_u32(&full[q % stages]), (q / stages) & 1);
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer.
-        const uint32_t idesc = f16_idesc(BM, BN);
+        // In a pair the even CTA's barriers count both CTAs' loads; the odd CTA waits until
+        // the MMAs that read its last loads are done.
+        for (int q = issued > stages ? issued - stages : 0; q < issued; ++q) {
+            if (pr == 0) (void)mbar_wait(smem_u32(&full[q % stages]), (q / stages) & 1);
+            else (void)mbar_wait(smem_u32(&empty[q % stages]), (q / stages) & 1);
+        }
+    } else if (warp == 1 && lane == 0 && pr == 0) {
+        // MMA issuer (in a pair, the even CTA's, for both).
+        const uint32_t idesc = f16_idesc(BM * kCta, BN);
         for (int i = 0, s = 0, ph = 0; i < n_kb; ++i) {
             if (!mbar_wait(smem_u32(&full[s]), ph)) {
                 atomicOr(status, kStatusTimeout);
@@ -169,17 +200,23 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
                 // Advancing 16 bf16 (32 B) along K inside the swizzled 128-byte row.
-                umma_bf16(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
-                          (i | k) != 0);
+                if constexpr (kPair)
+                    umma_bf16_pair(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
+                                   (i | k) != 0);
+                else
+                    umma_bf16(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
+                              (i | k) != 0);
             }
-            umma_commit(smem_u32(&empty[s]));
+            if constexpr (kPair) umma_commit_pair(smem_u32(&empty[s]), pair_mask);
+            else umma_commit(smem_u32(&empty[s]));
             if (++s == stages) {
                 s = 0;
                 ph ^= 1;
             }
         }
         // Signals once every MMA issued above has completed (also after a timeout).
-        umma_commit(smem_u32(accum));
+        if constexpr (kPair) umma_commit_pair(smem_u32(accum), pair_mask);
+        else umma_commit(smem_u32(accum));
     }
     __syncwarp();
 
@@ -226,15 +263,16 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
         // partials of the j-th other CTA (in split order), one padded row per tile row.
         // Barrier 1: every CTA of the cluster is done with its ring.
         cluster_sync();
-        const int me = (int)cluster_ctarank();
+        const int me = split;
         const int slice = BN / ks;                   // a multiple of 16
         if (ready) {
             for (int o = 0; o < ks; ++o) {
                 if (o == me) continue;
                 // In owner o's receive area, sender `me` uses slot me (or me - 1).
+                // The CTAs holding the same rows: cluster rank o * kCta + pr.
                 const uint32_t dst = mapa(smem_u32(smem) + (uint32_t)(me < o ? me : me - 1) *
                                               recv_slot_bytes(slice) + recv_offset(0, trow),
-                                          (uint32_t)o);
+                                          (uint32_t)(o * kCta + pr));
                 if constexpr (kMinBlocks == 1) {
                     for (int c = 0; c < slice; c += 16) {
                         uint32_t v[16];
@@ -313,11 +351,18 @@ projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_consta
     tc_fence_before();
     __syncthreads();
     if (done_counter != nullptr && threadIdx.x == 0) atomicAdd(done_counter, 1u);
+    // A pair frees its tensor memory together, once both CTAs have drained it.
+    if constexpr (kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(tmem_cols)
-                     : "memory");
+        if constexpr (kPair)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(tmem_cols)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(tmem_cols)
+                         : "memory");
     }
 }
 
@@ -359,81 +404,103 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
 }
 
 struct ProjPlan {
-    int BN = 0;             // N tile: the rank rounded up to 16, at most 256
+    bool pair = false;      // CTA pairs (cta_group::2): 256-row tiles over two CTAs
+    int BN = 0;             // N tile: the rank rounded up to 16 (32 for pairs), at most 256
     uint32_t tmem_cols = 0; // power of two >= max(32, BN)
     int stages = 0;         // ring stages
-    int ks = 1;             // K splits per tile = CTAs per cluster
-    int m_tiles = 0;
+    int ks = 1;             // K splits per tile
+    int m_tiles = 0;        // row tiles (of 128 rows, or 256 for pairs)
     int n_tiles = 0;
     size_t smem = 0;        // dynamic shared memory per CTA
+    int cluster() const { return ks * (pair ? 2 : 1); }
 };
 
 uint32_t recv_bytes(int BN, int ks) {
     return ks > 1 ? (uint32_t)(ks - 1) * recv_slot_bytes(BN / ks) : 0u;
 }
 
-size_t smem_bytes(int BN, int stages) {
-    return 1024 + (size_t)stages * (kATileBytes + (size_t)BN * BK * 2) +
+size_t smem_bytes(int bn_cta, int stages) {
+    return 1024 + (size_t)stages * (kATileBytes + (size_t)bn_cta * BK * 2) +
            (2 * stages + 1) * sizeof(uint64_t) + 16;
+}
+
+int ring_stages(int bn_cta) {
+    const uint32_t stage = kATileBytes + (uint32_t)bn_cta * BK * 2;
+    const int st = (int)(kRingBudget / stage);
+    return st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
 }
 
 // Largest dynamic shared memory any plan asks for (set once per device).
 size_t max_smem_bytes() {
     size_t m = 0;
-    for (int BN = 16; BN <= kMaxBN; BN += 16) {
-        const uint32_t stage = kATileBytes + (uint32_t)BN * BK * 2;
-        int st = (int)(kRingBudget / stage);
-        st = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
-        const size_t b = smem_bytes(BN, st);
+    for (int bn = 16; bn <= kMaxBN; bn += 16) {
+        const size_t b = smem_bytes(bn, ring_stages(bn));
         m = b > m ? b : m;
     }
     return m;
 }
 
-// Whether clusters of ks CTAs of this kernel, with smem bytes each, can be resident.
-bool cluster_fits(int device, int ks, size_t smem) {
+// Whether clusters of `size` CTAs of this kernel, with smem bytes each, can be resident.
+bool cluster_fits(int device, int size, bool pair, size_t smem) {
     static std::mutex mu;
-    static int cache[64][kMaxSplit + 1] = {{0}};   // 0 unknown, 1 fits, 2 does not
+    static int cache[64][2][2 * kMaxSplit + 1] = {{{0}}};   // 0 unknown, 1 fits, 2 does not
     std::lock_guard<std::mutex> lock(mu);
-    if (device < 0 || device >= 64) return false;
-    if (cache[device][ks] == 0) {
+    if (device < 0 || device >= 64 || size > 2 * kMaxSplit) return false;
+    int& c = cache[device][pair ? 1 : 0][size];
+    if (c == 0) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)ks;
+        attr[0].val.clusterDim.x = (unsigned)size;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3((unsigned)ks);
+        cfg.gridDim = dim3((unsigned)size);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, projection_kernel<16>, &cfg);
+        const cudaError_t e =
+            pair ? cudaOccupancyMaxActiveClusters(&n, projection_kernel<1, true>, &cfg)
+                 : cudaOccupancyMaxActiveClusters(&n, projection_kernel<16, false>, &cfg);
         if (e != cudaSuccess) (void)cudaGetLastError();
-        cache[device][ks] = (e == cudaSuccess && n > 0) ? 1 : 2;
+        c = (e == cudaSuccess && n > 0) ? 1 : 2;
     }
-    return cache[device][ks] == 1;
+    return c == 1;
 }
 
-ProjPlan projection_plan(const DeviceInfo& dev, int M, int H, int rank) {
+// Beside the top-k (the fused selector) the N tile stays at most 128 wide and CTAs work
+// alone: measured there on GB300, 256-wide tiles split over K made the whole fused step
+// slower (gemma_large 1183 -> 1195 us), although the projection alone is faster with them.
+// Elsewhere a rank of 256 runs on CTA pairs, which stage half the operand bytes per SM for
+// the same MMA work (gemma_large: main loop 20.3 -> 14.5 us per CTA); narrower tiles were
+// no faster with pairs (qwen_zipf 13 -> 15 us).
+ProjPlan projection_plan(const DeviceInfo& dev, int M, int H, int rank, bool beside_topk) {
     ProjPlan p;
-    p.BN = rank >= kMaxBN ? kMaxBN : ((rank + 15) / 16) * 16;
+    const int max_bn = beside_topk ? 128 : kMaxBN;
+    p.BN = rank >= max_bn ? max_bn : ((rank + 15) / 16) * 16;
+    const bool pair = !beside_topk && p.BN == kMaxBN;
+    p.pair = pair;
     p.n_tiles = (rank + p.BN - 1) / p.BN;
     p.tmem_cols = 32;
     while (p.tmem_cols < (uint32_t)p.BN) p.tmem_cols <<= 1;
-    const uint32_t stage = kATileBytes + (uint32_t)p.BN * BK * 2;
-    p.stages = (int)(kRingBudget / stage);
-    p.stages = p.stages < 2 ? 2 : (p.stages > kMaxStages ? kMaxStages : p.stages);
-    p.smem = smem_bytes(p.BN, p.stages);
-    p.m_tiles = (M + BM - 1) / BM;
+    const int bn_cta = pair ? p.BN / 2 : p.BN;
+    p.stages = ring_stages(bn_cta);
+    p.smem = smem_bytes(bn_cta, p.stages);
+    const int rows = pair ? 2 * BM : BM;
+    p.m_tiles = (M + rows - 1) / rows;
     const int nkb = (H + BK - 1) / BK;
-    const uint32_t ring = (uint32_t)p.stages * stage;
+    const uint32_t ring = (uint32_t)p.stages * (kATileBytes + (uint32_t)bn_cta * BK * 2);
+    const int cta = pair ? 2 : 1;
+    if (pair && !cluster_fits(dev.device, 2, true, p.smem))
+        return projection_plan(dev, M, H, rank, true);
     // Double the split while the tiles times the splits still fit in one wave, each split
     // keeps enough K blocks to run its pipeline, and each slice stays a multiple of 16 wide.
-    while (2 * p.ks <= kMaxSplit && (long long)p.m_tiles * p.n_tiles * 2 * p.ks <= dev.sm_count &&
+    while (2 * p.ks <= kMaxSplit &&
+           (long long)p.m_tiles * p.n_tiles * cta * 2 * p.ks <= dev.sm_count &&
            nkb >= 2 * p.ks * kMinKbPerSplit && p.BN % (2 * p.ks * 16) == 0 &&
-           recv_bytes(p.BN, 2 * p.ks) <= ring && cluster_fits(dev.device, 2 * p.ks, p.smem))
+           recv_bytes(p.BN, 2 * p.ks) <= ring &&
+           cluster_fits(dev.device, cta * 2 * p.ks, pair, p.smem))
         p.ks *= 2;
     return p;
 }
@@ -445,47 +512,56 @@ cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               uint32_t* status_word, cudaStream_t stream, bool beside_topk,
                               uint32_t* done_counter) {
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-    // Allow the largest layout once per device, for both builds; every plan fits under it.
+    // Allow the largest layout once per device, for every build; every plan fits under it.
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     std::call_once(once[dev.device], [&] {
         const int smem = (int)max_smem_bytes();
-        cudaError_t e = cudaFuncSetAttribute(projection_kernel<16>,
+        cudaError_t e = cudaFuncSetAttribute(projection_kernel<16, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(projection_kernel<1>,
+            e = cudaFuncSetAttribute(projection_kernel<1, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(projection_kernel<1, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         attr_err[dev.device] = e;
     });
     if (attr_err[dev.device] != cudaSuccess) return attr_err[dev.device];
-    const ProjPlan plan = projection_plan(dev, M, H, rank);
+    const ProjPlan plan = projection_plan(dev, M, H, rank, beside_topk);
     CUtensorMap map_a, map_b;
     if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
-        !encode_2d(&map_b, w_proj, (uint64_t)rank, (uint64_t)H, (uint32_t)plan.BN))
+        !encode_2d(&map_b, w_proj, (uint64_t)rank, (uint64_t)H,
+                   (uint32_t)(plan.pair ? plan.BN / 2 : plan.BN)))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)plan.ks;
+    attr[0].val.clusterDim.x = (unsigned)plan.cluster();
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)(plan.m_tiles * plan.ks), (unsigned)plan.n_tiles);
+    cfg.gridDim = dim3((unsigned)(plan.m_tiles * plan.cluster()), (unsigned)plan.n_tiles);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (beside_topk)
-        return cudaLaunchKernelEx(&cfg, projection_kernel<16>, map_a, map_b, h_out, M, rank, H,
-                                  plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word,
+        return cudaLaunchKernelEx(&cfg, projection_kernel<16, false>, map_a, map_b, h_out, M, rank,
+                                  H, plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word,
                                   done_counter);
-    return cudaLaunchKernelEx(&cfg, projection_kernel<1>, map_a, map_b, h_out, M, rank, H, plan.BN,
-                              plan.tmem_cols, plan.ks, plan.stages, status_word, done_counter);
+    if (plan.pair)
+        return cudaLaunchKernelEx(&cfg, projection_kernel<1, true>, map_a, map_b, h_out, M, rank,
+                                  H, plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word,
+                                  done_counter);
+    return cudaLaunchKernelEx(&cfg, projection_kernel<1, false>, map_a, map_b, h_out, M, rank, H,
+                              plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word,
+                              done_counter);
 }
 
 int projection_ctas(const DeviceInfo& dev, int M, int H, int rank) {
-    const ProjPlan plan = projection_plan(dev, M, H, rank);
-    return plan.m_tiles * plan.ks * plan.n_tiles;
+    const ProjPlan plan = projection_plan(dev, M, H, rank, true);
+    return plan.m_tiles * plan.cluster() * plan.n_tiles;
 }
 
 }  // namespace dflash

@@ -239,6 +239,9 @@ def _projection_case(dev, rows, H, rank, seed, what):
 @pytest.mark.parametrize("rows,H,rank", [
     (1, 8, 8), (129, 72, 24), (300, 1000, 256), (256, 64, 128), (17, 4096, 40),
     (1000, 5376, 256), (385, 3840, 128), (64, 2048, 136), (130, 520, 248),
+    # 256-wide N tiles run on CTA pairs (256-row tiles over two CTAs): a single row (the odd
+    # CTA's rows all out of range), a tail tile of one row, one K block, a K split.
+    (1, 64, 256), (257, 520, 256), (7680, 64, 256), (640, 2048, 256),
 ])
 def test_projection_shapes(dev, rows, H, rank):
     _projection_case(dev, rows, H, rank, rows + H + rank, f"rows={rows} H={H} rank={rank}")
