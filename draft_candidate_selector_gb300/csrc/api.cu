@@ -394,8 +394,10 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     queue.proj_ctas = dflash::projection_ctas(dev, R * S, H, rank);
     // Schedule, one stream. Each kernel is the next one's programmatic dependent: it may start
     // once every CTA of the kernel before it has started, and takes only the resources that
-    // kernel leaves. So the top-k runs beside the projection (one projection CTA per SM fits
-    // beside three top-k CTAs), and the edges take the SMs that top-k CTAs leave as they
+    // kernel leaves. So the top-k runs beside the projection (an SM holding a projection CTA
+    // takes one top-k CTA at once and two more when the projection CTA ends: its shared-memory
+    // configuration leaves room for only one more CTA), and the edges take the SMs that top-k
+    // CTAs leave as they
     // finish, each scoring a tile once the ready queue hands it over (its rows are written)
     // and the projection's count of finished CTAs is complete: most edges run in the top-k's
     // tail. No kernel waits for one that may not have started, so nothing can stall. A traced

@@ -85,9 +85,9 @@ cudaError_t topk_static_scratch(int device, void** ptr);
 
 // Returns cudaSuccess, or an error if the tensor maps cannot be encoded or the launch
 // fails. status_word receives kStatusTimeout if a bounded pipeline wait gives up.
-// beside_topk selects the build that keeps to 32 registers per thread, so that a projection
-// CTA fits on an SM beside three top-k CTAs (the fused selector's schedule), with N tiles at
-// most 128 wide. Below a rank of 256 both take the same plan and give identical bits; at 256
+// beside_topk selects the build that keeps to 32 registers per thread, so that by registers
+// a projection CTA fits on an SM beside three top-k CTAs (the fused selector's schedule),
+// with N tiles at most 128 wide. Below a rank of 256 both take the same plan and give identical bits; at 256
 // the other build runs CTA pairs with a K split, so its fp32 sums may round differently
 // (both stay within the accumulation bound of the exact product).
 // done_counter, if not null, is incremented by every CTA once its part of h is written and

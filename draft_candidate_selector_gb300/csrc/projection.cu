@@ -41,7 +41,8 @@
 // sets kStatusTimeout, skips the remaining work, still takes part in both cluster
 // barriers, frees its tensor memory, and returns.
 // The fused selector runs the projection beside the top-k: its build keeps to 32 registers
-// per thread, so that one projection CTA (128 threads) fits beside three top-k CTAs on an SM.
+// per thread, so that by registers one projection CTA (128 threads) fits beside three top-k
+// CTAs on an SM (65,536 registers exactly).
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -74,9 +75,9 @@ __host__ __device__ constexpr uint32_t recv_offset(int c, int row) {
     return (uint32_t)(c >> 2) * (BM * 16u) + (uint32_t)row * 16u;
 }
 
-// Two builds. kMinBlocks = 16 caps the registers at 32 per thread, so that one projection
-// CTA fits beside three top-k CTAs on an SM (the fused selector runs them side by side);
-// kMinBlocks = 1 leaves the compiler free, for calls where nothing runs beside it.
+// Two builds. kMinBlocks = 16 caps the registers at 32 per thread, so that by registers one
+// projection CTA fits beside three top-k CTAs on an SM (the fused selector runs them side by
+// side); kMinBlocks = 1 leaves the compiler free, for calls where nothing runs beside it.
 template <int kMinBlocks, bool kPair>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 projection_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
