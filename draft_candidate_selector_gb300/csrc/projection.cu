@@ -9,10 +9,11 @@
 // Linear [out, in]) are both K-major, which is the native operand form of tcgen05.mma.
 //
 // Tiling. The output is cut into 128 x BN tiles, BN = the rank rounded up to 16, at most
-// 256 (the widest N of one M = 128 tcgen05.mma). Wide tiles pay: measured on GB300, an
-// M = 128, K = 16 MMA takes about as long at N = 128 as at N = 256 (a CTA's chain of MMAs
-// with the loads taken out: 31 us for 84 K blocks at N = 128, 33 us at N = 256), so a
-// 128-wide tile does half the work per MMA. A cluster of `ks` CTAs computes one tile,
+// 256 (the widest N of one M = 128 tcgen05.mma). Wide tiles pay: measured on GB300, a CTA's
+// ring (wait for a stage, four M = 128, K = 16 MMAs, commit) takes about 0.42 us per K block
+// at N = 128 even with the loads taken out, while the same MMAs issued without the waits take
+// 0.17 us; at N = 256 the MMAs take 0.31 us and hide most of the ring's cost, so a 256-wide
+// tile does about twice the work per K block. A cluster of `ks` CTAs computes one tile,
 // splitting K: CTA s of the cluster (its cluster rank) takes the contiguous K blocks
 // [s * nkb / ks, (s + 1) * nkb / ks). The host doubles ks, from 1, while the tiles times ks
 // still fit the SMs in one wave and every split keeps at least 8 K blocks (gemma_large:
