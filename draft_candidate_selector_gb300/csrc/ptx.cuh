@@ -1,6 +1,7 @@
-// ptx.cuh: inline-PTX wrappers for the sm_100-family features the kernels use: mbarriers
-// with bounded waits, TMA tensor loads, tcgen05 MMA, commit and tensor-memory loads, and
-// the shared-memory and instruction descriptors of tcgen05.mma kind::f16.
+// ptx.cuh: inline-PTX wrappers for the Blackwell (sm_103a) features the kernels use: mbarriers
+// with bounded waits, TMA tensor loads (one CTA or a CTA pair), tcgen05 MMA and commit (one
+// CTA or a CTA pair), tensor-memory loads, thread-block cluster barriers and distributed shared
+// memory stores, and the shared-memory and instruction descriptors of tcgen05.mma kind::f16.
 #pragma once
 
 #include <cuda.h>
@@ -62,19 +63,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(map), "r"(bar), "r"(x), "r"(y)
         : "memory");
-}
-
-// Prefetch a tile of a tensor map into L2 (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// Prefetch `bytes` contiguous bytes of global memory into L2 (16-byte aligned address, size
-// a multiple of 16). No shared memory, nothing to wait for.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
