@@ -554,6 +554,31 @@ def test_selector_forward(dev, name):
     _status_clean()
 
 
+@pytest.mark.parametrize("R,S,K,V,H,rank", [(4, 15, 32, 50000, 5376, 256), (3, 7, 13, 40000, 520, 256)])
+def test_selector_forward_rank_256(dev, R, S, K, V, H, rank):
+    """The forward pass at a rank of 256, where the projection runs on CTA pairs with a K
+    split (the fused selector's build takes another plan there): h and the edge scores
+    against the oracle, with repeated candidates and an odd K."""
+    g = torch.Generator().manual_seed(R * 1000 + K)
+    hidden = torch.randn(R, S, H, generator=g).to(torch.bfloat16)
+    w_proj = (torch.randn(rank, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+    pred_cb = (torch.randn(V, rank, generator=g) / rank ** 0.5).to(torch.bfloat16)
+    succ_cb = (torch.randn(V, rank, generator=g) / rank ** 0.5).to(torch.bfloat16)
+    rng = np.random.default_rng(R + K)
+    cand = rng.integers(0, V, size=(R, S, K)).astype(np.int32)
+    cand[:, :, -1] = cand[:, :, 0]
+    unary = rng.standard_normal((R, S, K)).astype(np.float32)
+    anchors = rng.integers(0, V, size=(R,)).astype(np.int32)
+    h, e = ds.dflash_selector_forward(torch.from_numpy(cand).to(dev), torch.from_numpy(unary).to(dev),
+                                      hidden.to(dev), torch.from_numpy(anchors).to(dev),
+                                      w_proj.to(dev), pred_cb.to(dev), succ_cb.to(dev))
+    torch.cuda.synchronize(dev)
+    P.assert_projection(P.bits(h), P.bits(hidden), P.bits(w_proj), f"rank 256 forward h R={R} K={K}")
+    ref = oracle.edges(P.bits(pred_cb), P.bits(succ_cb), cand, unary, P.bits(h), anchors)
+    P.assert_close(e.cpu().numpy(), ref, f"rank 256 forward edges R={R} K={K}")
+    _status_clean()
+
+
 @pytest.mark.parametrize("name", SMALL + ["ragged"] + LARGE)
 def test_best_path(dev, name):
     """The best path through the fused selector's edge scores equals the oracle's (same fp32
