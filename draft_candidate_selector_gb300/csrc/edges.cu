@@ -20,7 +20,8 @@
 //      significant bits, and G = hi + lo exactly with hi = bf16(G), lo = bf16(G - hi).
 //      Both halves are multiplied (two MMAs), so each product is exact and the sums run
 //      in fp32. B fragments (successor rows) come from ldmatrix.
-//   3. Epilogue: add unary[c], store rows q < K, columns c < K.
+//   3. Epilogue: add unary[c], store rows q < K, columns c < K (a pair of columns per 8-byte
+//      store when K is even and the output 8-byte aligned).
 // In the forward pass (projection, then edges on one stream) the edges are launched as the
 // projection's programmatic dependent: their CTAs start on free SMs, issue the id loads and
 // codebook gathers, and wait (griddepcontrol.wait) for the projection only before copying h.
@@ -231,6 +232,9 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
     const int* bad_c = bad + kMaxK;
     float* out = edges + row * K * K;
     const float* un = unary + row * K;
+    // A candidate pair (c, c + 1) is stored with one 8-byte store when K is even and the
+    // output is 8-byte aligned (then every pair is); otherwise one value at a time.
+    const bool pair_store = (K & 1) == 0 && (reinterpret_cast<uintptr_t>(edges) & 7u) == 0;
     for (int item = warp; item < m_tiles * n_pairs; item += kWarps) {
         const int m0 = (item % m_tiles) * 16;
         const int n0 = (item / m_tiles) * 16;
@@ -269,18 +273,24 @@ edges_kernel(const uint16_t* __restrict__ pred_cb, const uint16_t* __restrict__ 
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int c = n0 + nt * 8 + 2 * t;
+            const int c = n0 + nt * 8 + 2 * t;           // even
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int q = m0 + g + half * 8;
-                if (q >= K) continue;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int cc = c + e;
-                    if (cc >= K) continue;
-                    float v = acc[nt][2 * half + e] + u[nt][e];
-                    if (bad_q[q] || bad_c[cc]) v = __int_as_float(0x7FC00000);
-                    out[q * K + cc] = v;
+                if (q >= K || c >= K) continue;
+                float v0 = acc[nt][2 * half] + u[nt][0];
+                float v1 = acc[nt][2 * half + 1] + u[nt][1];
+                if (bad_q[q] || bad_c[c]) v0 = __int_as_float(0x7FC00000);
+                if (pair_store) {
+                    // K even: c + 1 < K as well, and q * K + c is even.
+                    if (bad_q[q] || bad_c[c + 1]) v1 = __int_as_float(0x7FC00000);
+                    *reinterpret_cast<float2*>(out + q * K + c) = make_float2(v0, v1);
+                } else {
+                    out[q * K + c] = v0;
+                    if (c + 1 < K) {
+                        if (bad_q[q] || bad_c[c + 1]) v1 = __int_as_float(0x7FC00000);
+                        out[q * K + c + 1] = v1;
+                    }
                 }
             }
         }

@@ -320,6 +320,15 @@ def test_edges_shapes(dev, R, S, K, V, rank):
     # Structure that holds at any size: every predecessor row at step 0 is identical.
     e0 = e[:, 0]
     assert torch.equal(e0, e0[:, :1, :].expand_as(e0))
+    # The output only needs 4-byte alignment: written at an address that is not 8-byte
+    # aligned (one value at a time rather than in pairs), the scores are the same bits.
+    buf = torch.full((R * S * K * K + 1,), float("nan"), dtype=torch.float32, device=dev)
+    e_odd = buf[1:].view(R, S, K, K)
+    ds.dflash_candidate_edges(
+        pred.to(dev), succ.to(dev), torch.from_numpy(ids).to(dev), torch.from_numpy(un).to(dev),
+        torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(dev),
+        torch.from_numpy(anchors).to(dev), edges=e_odd)
+    assert torch.equal(e_odd.view(torch.int32), e.view(torch.int32))
     _status_clean()
 
 
