@@ -13,19 +13,27 @@
 // ring (wait for a stage, four M = 128, K = 16 MMAs, commit) takes about 0.42 us per K block
 // at N = 128 even with the loads taken out, while the same MMAs issued without the waits take
 // 0.17 us; at N = 256 the MMAs take 0.31 us and hide most of the ring's cost, so a 256-wide
-// tile does about twice the work per K block. A cluster of `ks` CTAs computes one tile,
-// splitting K: CTA s of the cluster (its cluster rank) takes the contiguous K blocks
-// [s * nkb / ks, (s + 1) * nkb / ks). The host doubles ks, from 1, while the tiles times ks
-// still fit the SMs in one wave and every split keeps at least 8 K blocks (gemma_large:
-// 60 tiles of 256 columns, ks = 2; gemma_softcap: 30 tiles, ks = 4; qwen_zipf: 8 tiles,
-// ks = 4). In each CTA:
+// tile does about twice the work per K block.
+// CTA pairs. Outside the fused selector a 256-wide tile runs on a pair of CTAs
+// (tcgen05.mma.cta_group::2, M = 256): each CTA stages its own 128 rows of A and half of B's
+// rows at the same shared-memory offsets, the even CTA issues the MMAs for both, and each
+// CTA's tensor memory holds its 128 rows of the accumulator. The odd CTA's TMA loads count
+// their bytes on the even CTA's barrier; commits arrive on both CTAs' barriers (multicast).
+// A pair stages half the operand bytes per SM for the same MMA work.
+// K split. A cluster of `ks` tiles' CTAs (times two for pairs) splits K: split s takes the
+// contiguous K blocks [s * nkb / ks, (s + 1) * nkb / ks). The host doubles ks, from 1, while
+// the CTAs still fit the SMs in one wave and every split keeps at least 8 K blocks
+// (gemma_large standalone: 30 pair tiles of 256 x 256, ks = 2, clusters of 4; beside the
+// top-k: 60 x 2 tiles of 128 x 128, ks = 1; gemma_softcap: 30 tiles, ks = 4; qwen_zipf: 8
+// tiles, ks = 4). In each CTA:
 //   * warp 0, one lane: TMA producer. Per 64-wide K block it loads a 128x64 A tile and a
 //     BNx64 B tile (128-byte swizzle) into a ring of `stages` shared-memory stages (192 KB:
 //     4 at BN = 256, 6 at BN = 128, up to 8). Completion is tracked on mbarriers by
 //     transaction bytes.
-//   * warp 1, one lane: MMA issuer. tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), M=128,
-//     N=BN, K=16, four per K block, accumulating in tensor memory. tcgen05.commit frees
-//     each stage and finally signals the accumulator.
+//   * warp 1, one lane: MMA issuer (in a pair, the even CTA's only). tcgen05.mma kind::f16
+//     (bf16 x bf16 -> fp32), M = 128 (256 for a pair), N = BN, K = 16, four per K block,
+//     accumulating in tensor memory. tcgen05.commit frees each stage and finally signals
+//     the accumulator.
 //   * warps 0-3: epilogue; thread t owns row t of the tile (tensor-memory lane t).
 //       ks = 1: tcgen05.ld 16 columns at a time (8 in the register-capped build), round
 //       to bf16, store.
