@@ -43,6 +43,7 @@ constexpr int kUnroll = 8;              // 128-bit loads per lane per group (4 K
 // 1137 us vs 1184 us, qwen_zipf 118 us vs 111 us.
 constexpr long long kSmallProblemBytes = 2LL << 30;
 constexpr long long kMinSpan = 1024;    // smallest span given to one warp
+constexpr long long kShortSpan = 4096;  // spans up to this long (4 groups) are "short"
 constexpr long long kSpanAlign = 128;   // spans start 512 bytes apart (on 512-byte boundaries
                                         // when the logits are 16-byte aligned)
 constexpr unsigned kFull = 0xffffffffu;
@@ -440,6 +441,11 @@ TopkPlan topk_plan(const DeviceInfo& dev, long long rows, int V) {
                                 resident_blocks_per_sm(dev.device, p.variant) * kWarpsPerBlock;
     long long span = (p.total + max_warps - 1) / max_warps;
     span = std::max(span, kMinSpan);
+    // A row split over many warps ends in a chain of merges, one L2 round trip per list, so
+    // short spans keep a row to about 8 warps (small_ties: 32 -> 8 warps a row, top-k 28 -> 22
+    // us). Longer spans are left alone: fewer warps would read more slowly (qwen_zipf at 16
+    // requests, 55 -> 61 us with the rule applied there too).
+    span = std::max(span, std::min((long long)V / 8, kShortSpan));
     span = (span + kSpanAlign - 1) / kSpanAlign * kSpanAlign;
     p.span = span;
     p.warps = (int)((p.total + span - 1) / span);
