@@ -10,10 +10,10 @@
 //
 // Tiling. The output is cut into 128 x BN tiles, BN = the rank rounded up to 16, at most
 // 256 (the widest N of one M = 128 tcgen05.mma). Wide tiles pay: measured on GB300, a CTA's
-// ring (wait for a stage, four M = 128, K = 16 MMAs, commit) takes about 0.42 us per K block
-// at N = 128 even with the loads taken out, while the same MMAs issued without the waits take
-// 0.17 us; at N = 256 the MMAs take 0.31 us and hide most of the ring's cost, so a 256-wide
-// tile does about twice the work per K block.
+// ring (wait for a stage, four M = 128, K = 16 MMAs, commit) takes about 0.31 us per K block
+// at N = 128 even with the loads taken out, while the same MMAs issued back to back take
+// 0.17 us; at N = 256 the MMAs take 0.31 us, as long as the ring, so a 256-wide tile does
+// about twice the work per K block.
 // CTA pairs. Outside the fused selector a 256-wide tile runs on a pair of CTAs
 // (tcgen05.mma.cta_group::2, M = 256): each CTA stages its own 128 rows of A and half of B's
 // rows at the same shared-memory offsets, the even CTA issues the MMAs for both, and each
