@@ -1,7 +1,9 @@
 """Benchmark of the GB300 DFlash2 candidate selector.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--e2e-steps E] [--no-cpu-baseline] [--no-per-workload]
+                    [--workload NAME] [--requests R] [--e2e-steps E] [--graph]
+                    [--no-cpu-baseline] [--no-per-workload]
+    python bench.py --forward | --lmhead [--sustained SECONDS] | --best-path  [--workload NAME]
 
 One step is one dflash_selector call over one batch of the workload: vocabulary top-k,
 hidden projection and edge scores, with every input already in HBM. The default
@@ -27,6 +29,11 @@ Rank 0 prints one JSON line. It holds:
     the HBM peak, and the CPU oracle timed over the whole workload.
 With torchrun (N > 1) every rank runs an independent replica on its own GPU and its own
 seed (weak scaling). The only collectives are a barrier and a max over ranks of the time.
+
+The other modes time one part alone: --forward the selector's forward pass (no logits),
+--lmhead the top-k straight from the LM head (with cuBLAS GEMM plus top-k beside it for
+context), --best-path the max-sum path through the edge scores. --graph replays the step from
+a CUDA graph; --requests takes the first R requests of the workload (small cases for ncu).
 
 --impl reference times the CPU oracle (the reference arm of this benchmark) on a bounded
 sample per step, on the host cores, and prints the same line with "impl": "reference".
