@@ -115,17 +115,20 @@ cudaError_t launch_edges(const DeviceInfo& dev, const uint16_t* pred_cb,
 
 // ---------------------------------------------------------------- LM head + top-k (lmhead.cu)
 
-// How the candidate head from the LM head is cut. One main CTA per (128-row tile, vocabulary
-// split). When the main CTAs leave SMs idle, helper CTAs take over the tail of every split's
-// vocabulary range: the main CTA stops at rows_per_helper / (rows_per_helper + 1) of its
-// range, and each helper walks the tails of rows_per_helper consecutive row tiles in turn.
+// How the candidate head from the LM head is cut. One main unit per (row unit, vocabulary
+// split); a unit is one CTA on a 128-row tile, or a CTA pair on 256 rows (two 128-row tiles).
+// When the main units leave SMs idle, helper units take over the tail of every split's
+// vocabulary range: the main unit stops at rows_per_helper / (rows_per_helper + 1) of its
+// range, and each helper walks the tails of rows_per_helper consecutive row units in turn.
 // The partial lists of a row tile are merged by whichever CTA finishes last.
 struct LmheadPlan {
-    int m_tiles = 0;           // ceil(rows / 128)
+    int pair = 0;              // 1: CTA pairs on 256-row units
+    int m_units = 0;           // row units: ceil(rows / 128), or ceil(rows / 256) for pairs
+    int m_tiles = 0;           // 128-row tiles: m_units, or 2 m_units for pairs
     int n_tiles = 0;           // ceil(V / 256)
-    int n_splits = 0;          // vocabulary ranges per row tile
-    int rows_per_helper = 0;   // row tiles per helper CTA (0: no helpers)
-    int helpers_per_split = 0; // ceil(m_tiles / rows_per_helper), or 0
+    int n_splits = 0;          // vocabulary ranges per row unit
+    int rows_per_helper = 0;   // row units per helper (0: no helpers)
+    int helpers_per_split = 0; // ceil(m_units / rows_per_helper), or 0
     int slots = 0;             // partial lists per row tile: n_splits, doubled with helpers
     int blocks = 0;            // CTAs launched
     size_t counter_bytes = 0;  // per-row-tile arrival counters, padded to 256 B

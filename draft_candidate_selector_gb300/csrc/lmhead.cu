@@ -24,6 +24,11 @@
 //     spends as many steps as its busiest row has survivors. Each survivor goes into the
 //     row's sorted list, held in registers (KC = 8, 16 or 32 entries, the smallest that holds
 //     K) and updated by a branch-free network of min/max steps.
+// Where no helpers are needed and the rows fill 256-row units well, the CTAs work in pairs
+// (cluster of 2, tcgen05.mma.cta_group::2, M = 256): each CTA stages its own 128 hidden rows
+// and half of the LM-head tile, the even CTA issues the MMAs for both, and each CTA's
+// epilogue reads its own rows from its own tensor memory. A pair stages 48 KB per SM per K
+// block instead of 96 KB for the same MMA work.
 // When the main CTAs (row tiles x splits) leave SMs idle, helper CTAs fill them: every main
 // CTA stops early in its vocabulary range, and each helper takes the remaining tails of a few
 // consecutive row tiles, one after the other. The helpers of a split walk the same vocabulary
@@ -84,6 +89,11 @@ __host__ __device__ inline LmSmem lm_smem_layout() {
     L.flag = L.slot + 8;                                 // "this CTA merges" flag
     L.total = L.flag + 8;
     return L;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
@@ -235,11 +245,11 @@ __device__ __forceinline__ void finish_segment(uint64_t (&lst)[KC], bool ok, int
     }
 }
 
-template <int KC>
+template <int KC, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, int M, int H, int V, int K,
-                   int m_tiles, int n_tiles, int n_splits, int rows_per_helper,
+                   int m_units, int n_tiles, int n_splits, int rows_per_helper,
                    int helpers_per_split, float softcap, float scale,
                    int32_t* __restrict__ cand_ids, float* __restrict__ unary,
                    uint32_t* __restrict__ counters, uint64_t* __restrict__ partials,
@@ -258,7 +268,10 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const Work wk = work_of(blockIdx.x, m_tiles, n_tiles, n_splits, rows_per_helper,
+    constexpr int kCta = kPair ? 2 : 1;
+    const int crank = kPair ? (int)cluster_ctarank() : 0;
+    const int pr = crank & (kCta - 1);               // CTA within the pair (0 issues the MMAs)
+    const Work wk = work_of(blockIdx.x / kCta, m_units, n_tiles, n_splits, rows_per_helper,
                             helpers_per_split);
     const int m_first = wk.m_first, n_seg = wk.n_seg, n_begin = wk.n_begin, T = wk.T;
     const int num_kb = (H + BK - 1) / BK;
@@ -270,7 +283,7 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), BM);        // every epilogue thread arrives
+            mbar_init(smem_u32(&tempty[b]), BM * kCta);  // every epilogue thread (of both CTAs)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
@@ -278,16 +291,26 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
         *merge_flag = 0;
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (kPair) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint16_t pair_mask = (uint16_t)(3u << (crank & ~1));
 
     if (warp == 0) {
         if (lane == 0) {
@@ -295,7 +318,7 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
             long long g = 0;
             bool ok = true;
             for (int tt = 0; tt < n_seg * T && ok; ++tt) {
-                const int m_tile = m_first + tt / T;
+                const int m_unit = m_first + tt / T;
                 const int n0 = (n_begin + tt % T) * BN;
                 for (int kb = 0; kb < num_kb; ++kb, ++g) {
                     const int s = (int)(g % kStages);
@@ -306,20 +329,35 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
                         break;
                     }
                     const uint32_t fb = smem_u32(&full[s]);
-                    mbar_expect_tx(fb, kATile + kBTile);
-                    tma_load_2d(smem_u32(smem + L.a + s * kATile), &map_a, fb, kb * BK, m_tile * BM);
-                    tma_load_2d(smem_u32(smem + L.b + s * kBTile), &map_b, fb, kb * BK, n0);
+                    if constexpr (kPair) {
+                        // Both CTAs' bytes count on the even CTA's barrier: its rows of A and
+                        // half of the LM-head tile each.
+                        const uint32_t lead = mapa(fb, (uint32_t)(crank & ~1));
+                        if (pr == 0) mbar_expect_tx(fb, 2u * (kATile + kBTile / 2));
+                        tma_load_2d_pair(smem_u32(smem + L.a + s * kATile), &map_a, lead, kb * BK,
+                                         (m_unit * 2 + pr) * BM);
+                        tma_load_2d_pair(smem_u32(smem + L.b + s * kBTile), &map_b, lead, kb * BK,
+                                         n0 + pr * (BN / 2));
+                    } else {
+                        mbar_expect_tx(fb, kATile + kBTile);
+                        tma_load_2d(smem_u32(smem + L.a + s * kATile), &map_a, fb, kb * BK, m_unit * BM);
+                        tma_load_2d(smem_u32(smem + L.b + s * kBTile), &map_b, fb, kb * BK, n0);
+                    }
                 }
             }
-            // Let the last loads land before this thread leaves the role.
+            // Let the last loads land before this thread leaves the role (in a pair the even
+            // CTA's barriers count both CTAs' loads; the odd CTA waits for the MMAs that read
+            // its last loads).
             const long long issued = g;
-            for (long long q = std::max(0LL, issued - kStages); q < issued; ++q)
-                (void)mbar_wait(smem_u32(&full[q % kStages]), (uint32_t)((q / kStages) & 1));
+            for (long long q = std::max(0LL, issued - kStages); q < issued; ++q) {
+                if (pr == 0) (void)mbar_wait(smem_u32(&full[q % kStages]), (uint32_t)((q / kStages) & 1));
+                else (void)mbar_wait(smem_u32(&empty[q % kStages]), (uint32_t)((q / kStages) & 1));
+            }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---- MMA issuer
-            const uint32_t idesc = f16_idesc(BM, BN);
+        if (lane == 0 && pr == 0) {
+            // ---- MMA issuer (in a pair, the even CTA's, for both)
+            const uint32_t idesc = f16_idesc(BM * kCta, BN);
             long long g = 0;
             bool ok = true;
             for (int tt = 0; tt < n_seg * T && ok; ++tt) {
@@ -342,12 +380,19 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
                     const uint32_t a0 = smem_u32(smem + L.a + s * kATile);
                     const uint32_t b0 = smem_u32(smem + L.b + s * kBTile);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_bf16(acc, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
-                                  (kb | k) != 0);
-                    umma_commit(smem_u32(&empty[s]));
+                    for (int k = 0; k < BK / 16; ++k) {
+                        if constexpr (kPair)
+                            umma_bf16_pair(acc, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32),
+                                           idesc, (kb | k) != 0);
+                        else
+                            umma_bf16(acc, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
+                                      (kb | k) != 0);
+                    }
+                    if constexpr (kPair) umma_commit_pair(smem_u32(&empty[s]), pair_mask);
+                    else umma_commit(smem_u32(&empty[s]));
                 }
-                umma_commit(smem_u32(&tfull[buf]));
+                if constexpr (kPair) umma_commit_pair(smem_u32(&tfull[buf]), pair_mask);
+                else umma_commit(smem_u32(&tfull[buf]));
             }
         }
     } else {
@@ -374,19 +419,29 @@ lmhead_topk_kernel(const __grid_constant__ CUtensorMap map_a,
                 scan_tile(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN),
                           (uint32_t)(n_begin + t) * BN, V, lst, thr_f);
                 tc_fence_before();
-                mbar_arrive(smem_u32(&tempty[buf]));
+                if (kPair && pr != 0)
+                    mbar_arrive_remote(mapa(smem_u32(&tempty[buf]), (uint32_t)(crank & ~1)));
+                else
+                    mbar_arrive(smem_u32(&tempty[buf]));
             }
-            finish_segment(lst, ok, m_first + sg, wk.slots, wk.slot, t_row, M, K, softcap, scale,
-                           merge_flag, cand_ids, unary, counters, partials);
+            finish_segment(lst, ok, (m_first + sg) * kCta + pr, wk.slots, wk.slot, t_row, M, K,
+                           softcap, scale, merge_flag, cand_ids, unary, counters, partials);
         }
     }
     tc_fence_before();
     __syncthreads();
+    // A pair frees its tensor memory together, once both CTAs are done with it.
+    if constexpr (kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols)
-                     : "memory");
+        if constexpr (kPair)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(kTmemCols)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(kTmemCols)
+                         : "memory");
     }
 }
 
@@ -427,64 +482,108 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
 
 }  // namespace
 
-LmheadPlan lmhead_plan(const DeviceInfo& dev, long long rows, int V) {
+namespace {
+
+// The plan for units of kCta CTAs (1: 128-row tiles; 2: CTA pairs on 256-row tiles).
+LmheadPlan plan_for(const DeviceInfo& dev, long long rows, int V, int kCta) {
     LmheadPlan p;
-    p.m_tiles = (int)((rows + BM - 1) / BM);
+    p.pair = kCta == 2 ? 1 : 0;
+    p.m_units = (int)((rows + BM * kCta - 1) / (BM * kCta));
+    p.m_tiles = p.m_units * kCta;
     p.n_tiles = (V + BN - 1) / BN;
-    // One wave: as many vocabulary splits as fit next to the row tiles on the SMs. Timed on
+    // One wave: as many vocabulary splits as fit next to the row units on the SMs. Timed on
     // GB300, this beat every other split count tried (1 to 38), also the ones that fill all
     // SMs in two waves: with every SM on the tensor cores the clock drops under the power
     // cap, and a second wave restarts the pipelines.
-    const int sms = std::max(1, dev.sm_count);
-    p.n_splits = std::max(1, std::min(p.n_tiles, sms / std::max(1, p.m_tiles)));
-    // Helpers for the SMs the main CTAs leave idle (gemma-like shapes: 60 row tiles x 2 splits
-    // leave 32 of 152). Only when each split is long enough to cut, and a helper's row count
-    // is small enough for the cut to pay.
-    const int spare = p.m_tiles <= sms ? sms - p.m_tiles * p.n_splits : 0;
+    const int slots_on_chip = std::max(1, dev.sm_count / kCta);
+    p.n_splits = std::max(1, std::min(p.n_tiles, slots_on_chip / std::max(1, p.m_units)));
+    // Helpers for the unit slots the main units leave idle (gemma-like shapes: 60 row tiles x 2
+    // splits leave 32 of 152 SMs). Only when each split is long enough to cut, and a helper's
+    // row count is small enough for the cut to pay.
+    const int spare = p.m_units <= slots_on_chip ? slots_on_chip - p.m_units * p.n_splits : 0;
     const int g_max = spare / p.n_splits;
     if (g_max > 0 && p.n_tiles / p.n_splits >= kMinHelperTiles) {
-        const int r = (p.m_tiles + g_max - 1) / g_max;
+        const int r = (p.m_units + g_max - 1) / g_max;
         if (r <= kMaxHelperRows) {
             p.rows_per_helper = r;
-            p.helpers_per_split = (p.m_tiles + r - 1) / r;
+            p.helpers_per_split = (p.m_units + r - 1) / r;
         }
     }
     p.slots = p.rows_per_helper > 0 ? 2 * p.n_splits : p.n_splits;
-    p.blocks = p.m_tiles * p.n_splits + p.n_splits * p.helpers_per_split;
+    p.blocks = kCta * (p.m_units * p.n_splits + p.n_splits * p.helpers_per_split);
     p.counter_bytes = (size_t)((p.m_tiles * 4 + 255) / 256 * 256);
     p.partial_bytes = p.slots > 1 ? (size_t)p.m_tiles * p.slots * kMaxK * BM * 8 : 0;
     return p;
+}
+
+}  // namespace
+
+// CTA pairs stage half the LM-head bytes per SM for the same MMA work. Measured on GB300
+// (same ids bit for bit): faster where no helpers are needed (qwen_zipf 0.385 -> 0.370 ms,
+// gemma_softcap 4.37 -> 4.27 ms sustained), slower where helpers take the tails of the
+// vocabulary ranges (gemma_large 12.8 -> 13.3 ms), so pairs are used only without helpers,
+// and only when 256-row units pad the rows by at most an eighth.
+LmheadPlan lmhead_plan(const DeviceInfo& dev, long long rows, int V) {
+    const LmheadPlan single = plan_for(dev, rows, V, 1);
+    if (single.rows_per_helper > 0) return single;
+    const LmheadPlan pair = plan_for(dev, rows, V, 2);
+    const long long padding = (long long)pair.m_units * 2 * BM - rows;
+    if (pair.rows_per_helper > 0 || padding * 8 > rows) return single;
+    return pair;
 }
 
 cudaError_t launch_lmhead_topk(const DeviceInfo& dev, const LmheadPlan& plan, const uint16_t* hidden,
                                const uint16_t* lm_head, int M, int H, int V, int K, float softcap,
                                float scale, int32_t* cand_ids, float* unary, void* workspace,
                                uint32_t* status_word, cudaStream_t stream) {
-    static std::once_flag once[3][64];
-    static cudaError_t attr_err[3][64];
+    static std::once_flag once[2][3][64];
+    static cudaError_t attr_err[2][3][64];
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     // The register list holds KC >= K entries: the smallest build of 8, 16 or 32.
     const int kc = K <= 8 ? 0 : (K <= 16 ? 1 : 2);
-    auto kernel = kc == 0 ? lmhead_topk_kernel<8> : (kc == 1 ? lmhead_topk_kernel<16>
-                                                              : lmhead_topk_kernel<32>);
+    const int kp = plan.pair ? 1 : 0;
+    auto kernel = kp == 0 ? (kc == 0 ? lmhead_topk_kernel<8, false>
+                                     : (kc == 1 ? lmhead_topk_kernel<16, false>
+                                                : lmhead_topk_kernel<32, false>))
+                          : (kc == 0 ? lmhead_topk_kernel<8, true>
+                                     : (kc == 1 ? lmhead_topk_kernel<16, true>
+                                                : lmhead_topk_kernel<32, true>));
     const size_t smem = 1024 + lm_smem_layout().total;
-    std::call_once(once[kc][dev.device], [&] {
-        attr_err[kc][dev.device] = cudaFuncSetAttribute(
+    std::call_once(once[kp][kc][dev.device], [&] {
+        attr_err[kp][kc][dev.device] = cudaFuncSetAttribute(
             kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
-    if (attr_err[kc][dev.device] != cudaSuccess) return attr_err[kc][dev.device];
+    if (attr_err[kp][kc][dev.device] != cudaSuccess) return attr_err[kp][kc][dev.device];
     CUtensorMap map_a, map_b;
     if (!encode_2d(&map_a, hidden, (uint64_t)M, (uint64_t)H, BM) ||
-        !encode_2d(&map_b, lm_head, (uint64_t)V, (uint64_t)H, BN))
+        !encode_2d(&map_b, lm_head, (uint64_t)V, (uint64_t)H, plan.pair ? BN / 2 : BN))
         return cudaErrorInvalidValue;
     uint32_t* counters = static_cast<uint32_t*>(workspace);
     uint64_t* partials = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + plan.counter_bytes);
     cudaError_t err = cudaMemsetAsync(counters, 0, plan.counter_bytes, stream);
     if (err != cudaSuccess) return err;
-    kernel<<<plan.blocks, kThreads, smem, stream>>>(
-        map_a, map_b, M, H, V, K, plan.m_tiles, plan.n_tiles, plan.n_splits, plan.rows_per_helper,
-        plan.helpers_per_split, softcap, scale, cand_ids, unary, counters, partials, status_word);
-    return cudaGetLastError();
+    if (!plan.pair) {
+        kernel<<<plan.blocks, kThreads, smem, stream>>>(
+            map_a, map_b, M, H, V, K, plan.m_units, plan.n_tiles, plan.n_splits,
+            plan.rows_per_helper, plan.helpers_per_split, softcap, scale, cand_ids, unary,
+            counters, partials, status_word);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)plan.blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, M, H, V, K, plan.m_units, plan.n_tiles,
+                              plan.n_splits, plan.rows_per_helper, plan.helpers_per_split, softcap,
+                              scale, cand_ids, unary, counters, partials, status_word);
 }
 
 }  // namespace dflash

@@ -693,13 +693,19 @@ def _bf16(t):
     (7, 64, 300, 4),          # one row tile, two vocabulary tiles
     (130, 520, 8000, 8),      # ragged rows, K and V; 32 vocabulary splits of one tile each
     (300, 256, 3000, 32),     # K = 32
-    (2560, 64, 20000, 16),    # 20 row tiles, 7 splits: about 11 tiles per CTA
+    (2560, 64, 20000, 16),    # on 152 SMs: CTA pairs, 10 units of 256 rows x 7 splits
     (50, 64, 200, 20),        # one vocabulary tile: no split, no merge; K between list sizes
     (40, 128, 1500, 12),      # K between list sizes, ragged last chunk of 32 columns
     # On 152 SMs: 40 row tiles x 3 splits plus 30 helper CTAs (4 row tiles' tails each)
     (5000, 64, 6000, 8),
     # On 152 SMs: 100 row tiles x 1 split plus 50 helpers (2 tails each): two lists per row
     (12700, 64, 2100, 32),
+    # Single CTAs, 9 row tiles x 16 splits (pairs would pad the rows by a sixth)
+    (1100, 64, 20000, 16),
+    # CTA pairs, 5 row units x 15 splits; the odd CTA of the last pair holds padding only
+    (1152, 96, 9000, 32),
+    # CTA pairs, 4 row units x 19 splits, the last unit a quarter padding; K = 8
+    (960, 128, 11000, 8),
 ])
 def test_lmhead_topk_valid(dev, rows, H, V, K):
     g = torch.Generator().manual_seed(rows + V)
@@ -733,10 +739,12 @@ def test_lmhead_topk_full_size_sampled(dev, name):
     _status_clean()
 
 
-def test_lmhead_topk_one_hot_exact(dev):
+@pytest.mark.parametrize("rows", [200, 1024])
+def test_lmhead_topk_one_hot_exact(dev, rows):
     """One-hot hidden states make every logit an exact LM-head entry: no rounding at all, so
-    the ids must equal the oracle's, ties (planted in the LM head) included."""
-    rows, H, V, K = 200, 128, 5000, 16
+    the ids must equal the oracle's, ties (planted in the LM head) included. 1024 rows run on
+    CTA pairs (4 row units of 256 x 19 vocabulary splits on 152 SMs)."""
+    H, V, K = 128, 5000, 16
     rng = np.random.default_rng(5)
     hot = rng.integers(0, H, rows)
     x = np.zeros((1, rows, H), dtype=np.float32)
@@ -799,6 +807,7 @@ def test_lmhead_odd_k_request_slices(dev):
 @pytest.mark.parametrize("R,S,K,V,H,rank,cap,scale", [
     (3, 7, 8, 5000, 256, 64, 0.0, 1.0),        # 21 rows, 20 vocabulary splits
     (40, 15, 32, 6000, 128, 128, 30.0, 1.5),   # 600 rows in 5 row tiles, K = 32, processed
+    (64, 16, 16, 7000, 192, 64, 30.0, 1.0),    # 1024 rows on CTA pairs (152 SMs), soft cap
 ])
 def test_selector_lmhead(dev, R, S, K, V, H, rank, cap, scale):
     """The draft step from the LM head: its candidates are those of dflash_lmhead_topk (same
