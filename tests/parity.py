@@ -160,6 +160,64 @@ def assert_lmhead_valid(gpu_ids: np.ndarray, gpu_unary: np.ndarray, hidden_bits:
     return same / gi.shape[0]
 
 
+def assert_lmhead_valid_every_row(ids: torch.Tensor, unary: torch.Tensor, hidden: torch.Tensor,
+                                  lm_head: torch.Tensor, K: int, what: str,
+                                  softcap: float = 0.0, scale: float = 1.0,
+                                  chunk: int = 256) -> None:
+    """Every row of an LM-head top-k at full size, against plain fp32 logits on the device.
+
+    The reference f is torch's fp32 GEMM of the bf16 inputs widened to fp32 (TF32 off): each
+    product is exact and only the fp32 sums round, as in the kernel. With
+    t_v = 2 * H * 2^-24 * sum_i |x_i w_vi| (the tolerance of assert_lmhead_valid), the
+    kernel's sum k_v and f_v each lie within t_v / 2 of the exact logit. The kernel keeps
+    k_v <= k_c for every v left out and c chosen, so f_v - t_v <= f_c + t_c. Checked on every
+    row, with a factor 2 of margin on t:
+    (a) the ids are in range and distinct;
+    (b) max over left-out v of (f_v - 2 t_v) <= min over chosen c of (f_c + 2 t_c);
+    (c) the unary values are non-increasing, and equal raw values keep ids ascending;
+    (d) each unary value is within 2 scale t_c (plus 1e-5 relative, the fp32 soft cap) of the
+        processed reference logit of its id.
+    """
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        H = hidden.shape[-1]
+        V = lm_head.shape[0]
+        x = hidden.reshape(-1, H)
+        n = x.shape[0]
+        gi = ids.reshape(n, K).long()
+        gu = unary.reshape(n, K).float()
+        assert bool(((gi >= 0) & (gi < V)).all()), f"{what}: an id out of range"
+        srt = gi.sort(dim=1).values
+        assert bool((srt[:, 1:] != srt[:, :-1]).all()), f"{what}: a row repeats an id"
+        assert bool((gu[:, 1:] <= gu[:, :-1]).all()), f"{what}: unary values not non-increasing"
+        if softcap == 0.0 and scale == 1.0:
+            tie = gu[:, 1:] == gu[:, :-1]
+            assert bool((~tie | (gi[:, 1:] > gi[:, :-1])).all()), \
+                f"{what}: equal values out of id order"
+        w32 = lm_head.float()
+        wabs = w32.abs()
+        for r0 in range(0, n, chunk):
+            xc = x[r0:r0 + chunk].float()
+            f = xc @ w32.t()                                           # [rows, V] fp32
+            t = (2.0 * H * 2.0 ** -24) * (xc.abs() @ wabs.t())         # [rows, V]
+            ic = gi[r0:r0 + chunk]
+            fc, tc = f.gather(1, ic), t.gather(1, ic)
+            low = f - 2.0 * t
+            low.scatter_(1, ic, float("-inf"))
+            bad = low.max(dim=1).values > (fc + 2.0 * tc).min(dim=1).values
+            assert not bool(bad.any()), \
+                f"{what}: row {r0 + int(bad.nonzero()[0])} left out a clear winner"
+            ref_u = (softcap * torch.tanh(fc / softcap) if softcap > 0 else fc) * scale
+            uc = gu[r0:r0 + chunk]
+            off = (uc - ref_u).abs() > 2.0 * scale * tc + 1e-5 * (1 + ref_u.abs())
+            assert not bool(off.any()), \
+                f"{what}: row {r0 + int(off.nonzero()[0, 0])} unary off the reference"
+            del f, t, low
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def float_bits(x: np.ndarray) -> np.ndarray:
     """bf16 bits of float32 values that are exactly representable in bf16 (checked)."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)

@@ -718,24 +718,42 @@ def test_lmhead_topk_valid(dev, rows, H, V, K):
     _status_clean()
 
 
-@pytest.mark.parametrize("name", ["qwen_zipf", "gemma_large"])
-def test_lmhead_topk_full_size_sampled(dev, name):
-    """At the full sizes the benchmark times, in the launch configuration it times (on 152 SMs:
-    qwen_zipf 8 row tiles x 19 splits, the last tile half padding; gemma_large 60 x 2 splits
-    plus 30 helper CTAs), sampled rows against the exact logits of the oracle."""
+def _lmhead_full_size(dev, name):
     w = wl.WORKLOADS[name]
     hid = wl._bf16_normal(0, wl._TAG_HIDDEN, (w.R, w.S, w.H), 1.0)
     g = torch.Generator(device=dev)
     g.manual_seed(1)
     lm = (torch.randn((w.V, w.H), generator=g, device=dev) / w.H ** 0.5).to(torch.bfloat16)
-    ids, un = ds.dflash_lmhead_topk(hid.to(dev), lm, w.K)
+    ids, un = ds.dflash_lmhead_topk(hid.to(dev), lm, w.K, softcap=w.softcap)
+    return w, hid, lm, ids, un
+
+
+@pytest.mark.parametrize("name", ["qwen_zipf", "gemma_softcap", "gemma_large"])
+def test_lmhead_topk_full_size_sampled(dev, name):
+    """At the full sizes the benchmark times, in the launch configuration it times (on 152 SMs:
+    qwen_zipf 4 CTA pairs of 256 rows x 19 splits, the last unit a quarter padding;
+    gemma_softcap 15 pairs x 5 splits, with the soft cap; gemma_large 60 single CTAs x 2
+    splits plus 30 helper CTAs), sampled rows against the exact logits of the oracle."""
+    w, hid, lm, ids, un = _lmhead_full_size(dev, name)
     last = w.rows - 1
-    rows = P.sample_rows(w.rows, 4, seed=11, extra=[127, 128, last - 128, last - 1])
+    rows = P.sample_rows(w.rows, 4, seed=11, extra=[127, 128, 255, 256, last - 128, last - 1])
     ids = ids.cpu().numpy().reshape(-1, w.K)[rows]
     un = un.cpu().numpy().reshape(-1, w.K)[rows]
     hb = P.bits(hid).reshape(-1, w.H)[rows]
-    same = P.assert_lmhead_valid(ids, un, hb, P.bits(lm), w.K, f"{name} sampled rows")
+    same = P.assert_lmhead_valid(ids, un, hb, P.bits(lm), w.K, f"{name} sampled rows",
+                                 softcap=w.softcap)
     assert same >= 0.5, f"only {same:.2f} of the sampled rows match the exact order"
+    _status_clean()
+
+
+@pytest.mark.parametrize("name", ["qwen_zipf", "gemma_softcap", "gemma_large"])
+def test_lmhead_topk_full_size_every_row(dev, name):
+    """Every row at full size, against plain fp32 logits on the device (torch's GEMM of the
+    same bf16 inputs): ids valid and distinct, no clear winner left out, values ordered and
+    within the fp32 summation bound of the reference."""
+    w, hid, lm, ids, un = _lmhead_full_size(dev, name)
+    P.assert_lmhead_valid_every_row(ids, un, hid.to(dev), lm, w.K, f"{name} every row",
+                                    softcap=w.softcap)
     _status_clean()
 
 
