@@ -358,6 +358,12 @@ def measure_forward(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, pe
         for _ in range(warmup):
             fn()
         out[f"{name}_ms"] = timed_calls(fn, steps, stream, flush)
+    # The fixed cost of any launch timed this way: a one-CTA kernel that writes 4 bytes,
+    # between the same two events after the same flush.
+    tiny = torch.zeros(1, dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        tiny.zero_()
+    out["launch_floor_ms"] = timed_calls(tiny.zero_, steps, stream, flush)
     b = w.algorithmic_bytes()
     proj_bytes = b["hidden"] + b["w_proj"] + b["h_out"]
     proj_flops = 2.0 * w.rows * w.H * w.rank
@@ -369,8 +375,11 @@ def measure_forward(ds, w: wl.Workload, dev, stream, steps: int, warmup: int, pe
                  else "tensor",
         "algorithmic_bytes": proj_bytes, "flops": proj_flops, "bound_ms": bound_ms,
         "frac": bound_ms / out["projection_ms"],
+        "frac_net_of_launch_floor": bound_ms / max(out["projection_ms"] - out["launch_floor_ms"], 1e-9),
+        "best_frac_with_launch_floor": bound_ms / (bound_ms + out["launch_floor_ms"]),
         "what": "max(bytes / HBM peak, FLOPs / bf16 burst peak), both measured, over the "
-                "projection's time"}
+                "projection's time; net of the launch floor, and the best a kernel at the "
+                "bound could show measured this way"}
     out["l2"] = "L2 flushed before every call (a buffer of twice the L2 read)"
     del flush
     return out
