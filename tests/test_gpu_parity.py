@@ -777,6 +777,29 @@ def test_lmhead_topk_one_hot_exact(dev, rows):
     _status_clean()
 
 
+def test_lmhead_topk_fuzz_shapes(dev):
+    """Seeded random shapes, most of them in the CTA-pair regime on 152 SMs (rows a multiple
+    of 256 or close below one, no helper CTAs): ragged vocabularies (the odd CTA's half of the
+    last vocabulary tile out of range), hidden sizes that are not a multiple of the 64-wide K
+    block, K from 1 to 32, with and without the logits processor. Every row is checked
+    against plain fp32 logits on the device."""
+    rng = np.random.default_rng(2024)
+    for case in range(8):
+        rows = int(rng.choice([512, 1000, 1024, 1536, 1800, 2048, 700, 256]))
+        V = int(rng.integers(300, 12000))
+        H = int(rng.integers(1, 80)) * 8
+        K = int(rng.integers(1, 33))
+        cap, scale = [(0.0, 1.0), (20.0, 0.75)][case % 2]
+        g = torch.Generator().manual_seed(case)
+        hid = _bf16(torch.randn(1, rows, H, generator=g)).to(dev)
+        w = _bf16(torch.randn(V, H, generator=g) / H ** 0.5).to(dev)
+        ids, un = ds.dflash_lmhead_topk(hid, w, K, softcap=cap, scale=scale)
+        P.assert_lmhead_valid_every_row(ids, un, hid, w, K,
+                                        f"rows={rows} H={H} V={V} K={K} cap={cap}",
+                                        softcap=cap, scale=scale)
+    _status_clean()
+
+
 def test_lmhead_topk_logits_processor(dev):
     g = torch.Generator().manual_seed(3)
     rows, H, V, K = 64, 96, 2000, 8
