@@ -27,8 +27,8 @@
 // Where no helpers are needed and the rows fill 256-row units well, the CTAs work in pairs
 // (cluster of 2, tcgen05.mma.cta_group::2, M = 256): each CTA stages its own 128 hidden rows
 // and half of the LM-head tile, the even CTA issues the MMAs for both, and each CTA's
-// epilogue reads its own rows from its own tensor memory. A pair stages 48 KB per SM per K
-// block instead of 96 KB for the same MMA work.
+// epilogue reads its own rows from its own tensor memory. Per K block a pair stages 64 KB
+// (32 KB per SM) where two single CTAs stage 96 KB, for the same MMA work.
 // When the main CTAs (row tiles x splits) leave SMs idle, helper CTAs fill them: every main
 // CTA stops early in its vocabulary range, and each helper takes the remaining tails of a few
 // consecutive row tiles, one after the other. The helpers of a split walk the same vocabulary
@@ -519,10 +519,11 @@ LmheadPlan plan_for(const DeviceInfo& dev, long long rows, int V, int kCta) {
 }  // namespace
 
 // CTA pairs stage half the LM-head bytes per SM for the same MMA work. Measured on GB300
-// (same ids bit for bit): faster where no helpers are needed (qwen_zipf 0.385 -> 0.370 ms,
-// gemma_softcap 4.37 -> 4.27 ms sustained), slower where helpers take the tails of the
-// vocabulary ranges (gemma_large 12.8 -> 13.3 ms), so pairs are used only without helpers,
-// and only when 256-row units pad the rows by at most an eighth.
+// (same ids bit for bit): faster where no helpers are needed (qwen_zipf 0.384 -> 0.372 ms,
+// gemma_softcap 4.42 -> 4.30 ms sustained), no faster where helpers take the tails of the
+// vocabulary ranges (gemma_large sustained: 12.8-12.9 -> 13.3 ms on one GPU, a tie on
+// another), so pairs are used only without helpers, and only when 256-row units pad the rows
+// by at most an eighth.
 LmheadPlan lmhead_plan(const DeviceInfo& dev, long long rows, int V) {
     const LmheadPlan single = plan_for(dev, rows, V, 1);
     if (single.rows_per_helper > 0) return single;
