@@ -18,6 +18,11 @@
 
 namespace {
 
+// In the fused selector, a projection of more than this many FLOPs is launched before the
+// top-k, a smaller one after it (see dflash_selector). The measured cases on either side:
+// 3.8 GFLOP (gemma_softcap) and 21.1 GFLOP (gemma_large).
+constexpr double kProjectionFirstFlops = 8e9;
+
 thread_local std::string g_last_error;
 
 dflash_status fail(dflash_status s, const char* fmt, ...) {
@@ -394,27 +399,48 @@ dflash_status dflash_selector(const float* logits, const uint16_t* hidden, const
     queue.proj_ctas = dflash::projection_ctas(dev, R * S, H, rank);
     // Schedule, one stream. Each kernel is the next one's programmatic dependent: it may start
     // once every CTA of the kernel before it has started, and takes only the resources that
-    // kernel leaves. So the top-k runs beside the projection (an SM holding a projection CTA
-    // takes one top-k CTA at once and two more when the projection CTA ends: its shared-memory
-    // configuration leaves room for only one more CTA), and the edges take the SMs that top-k
-    // CTAs leave as they
+    // kernel leaves. The edges come last and take the SMs that top-k CTAs leave as they
     // finish, each scoring a tile once the ready queue hands it over (its rows are written)
     // and the projection's count of finished CTAs is complete: most edges run in the top-k's
-    // tail. No kernel waits for one that may not have started, so nothing can stall. A traced
-    // call (dflash_trace_begin) records events between the kernels, which then run one after
-    // another, so that each can be timed.
+    // tail. The projection comes first when it is large (more than kProjectionFirstFlops):
+    // it then runs beside the top-k (an SM holding a projection CTA takes one top-k CTA at
+    // once and two more when the projection CTA ends: its shared-memory configuration leaves
+    // room for only one more CTA) and h is ready long before the edges need it. A smaller
+    // projection comes after the top-k instead and runs on the SMs the top-k's first finished
+    // CTAs leave, so every top-k CTA starts at once. Measured on GB300 (same bits either way):
+    // gemma_large (21.1 GFLOP of projection) 1174-1176 us projection first against 1205 us
+    // after; gemma_softcap (3.8 GFLOP) 589-590 -> 585.5-585.7 us, qwen_zipf 122.7-123.0 ->
+    // 119.1-119.4 us, small_ties 28.7-28.9 -> 27.2-27.5 us, tiny 17.4-18.7 -> 17.2 us with the
+    // projection after the top-k. Either way every producer a wait depends on has all its CTAs
+    // resident before any edge CTA exists, so nothing can stall. A traced call
+    // (dflash_trace_begin) records events between the kernels, which then run one after
+    // another in the first order, so that each can be timed.
     const bool chain = ev == nullptr;
+    const double proj_flops = 2.0 * (double)rows * (double)H * (double)rank;
+    const bool topk_first = chain && proj_flops <= kProjectionFirstFlops;
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "trace event");
     if ((e = cudaMemsetAsync(workspace, 0, plan.counter_bytes + qbytes, st)) != cudaSuccess)
         return cuda_fail(e, "clearing the workspace");
-    e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st,
-                                  /*beside_topk=*/true, queue.proj_done);
-    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "trace event");
-    e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale,
-                            qbytes, /*clear_counters=*/false, queue, /*programmatic=*/chain);
-    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    if (topk_first) {
+        e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap, scale,
+                                qbytes, /*clear_counters=*/false, queue, /*programmatic=*/false);
+        if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+        e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st,
+                                      /*beside_topk=*/true, queue.proj_done,
+                                      /*programmatic=*/true);
+        if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    } else {
+        e = dflash::launch_projection(dev, hidden, w_proj, R * S, H, rank, h_out, status, st,
+                                      /*beside_topk=*/true, queue.proj_done);
+        if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+        if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess)
+            return cuda_fail(e, "trace event");
+        e = dflash::launch_topk(plan, logits, V, K, cand_ids, unary, workspace, st, softcap,
+                                scale, qbytes, /*clear_counters=*/false, queue,
+                                /*programmatic=*/chain);
+        if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    }
     if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "trace event");
     e = dflash::launch_edges(dev, pred_cb, succ_cb, cand_ids, unary, h_out, anchors, R, S, K, V,
                              rank, edges, status, st, /*after_h_producer=*/false, queue,

@@ -96,7 +96,8 @@ cudaError_t topk_static_scratch(int device, void** ptr);
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank,
                               uint16_t* h_out, uint32_t* status_word, cudaStream_t stream,
-                              bool beside_topk = false, uint32_t* done_counter = nullptr);
+                              bool beside_topk = false, uint32_t* done_counter = nullptr,
+                              bool programmatic = false);
 int projection_ctas(const DeviceInfo& dev, int M, int H, int rank);
 
 // ---------------------------------------------------------------- edges (edges.cu)

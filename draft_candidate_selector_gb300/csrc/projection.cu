@@ -520,7 +520,7 @@ ProjPlan projection_plan(const DeviceInfo& dev, int M, int H, int rank, bool bes
 cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                               const uint16_t* w_proj, int M, int H, int rank, uint16_t* h_out,
                               uint32_t* status_word, cudaStream_t stream, bool beside_topk,
-                              uint32_t* done_counter) {
+                              uint32_t* done_counter, bool programmatic) {
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     // Allow the largest layout once per device, for every build; every plan fits under it.
     static std::once_flag once[64];
@@ -545,17 +545,22 @@ cudaError_t launch_projection(const DeviceInfo& dev, const uint16_t* hidden,
                    (uint32_t)(plan.pair ? plan.BN / 2 : plan.BN)))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)plan.cluster();
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // As the programmatic dependent of the kernel before it (the top-k of the fused selector),
+    // the projection may start once that kernel's CTAs have all started. It reads nothing that
+    // kernel writes, so it never waits for it.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)(plan.m_tiles * plan.cluster()), (unsigned)plan.n_tiles);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = programmatic ? 2 : 1;
     if (beside_topk)
         return cudaLaunchKernelEx(&cfg, projection_kernel<16, false>, map_a, map_b, h_out, M, rank,
                                   H, plan.BN, plan.tmem_cols, plan.ks, plan.stages, status_word,
