@@ -194,9 +194,12 @@ dflash_status dflash_candidate_edges(const uint16_t* pred_cb, const uint16_t* su
 
 /* ------------------------------------------------------------------------------------
  * The whole selector in one call, with no host round trip. All three steps run on `stream`,
- * each kernel launched as the programmatic dependent of the one before it: the top-k (step 1)
- * runs beside the projection (step 2), and the edges (step 3) take the SMs the top-k leaves as
- * it finishes, scoring each (r, p) tile as soon as the top-k has written the rows it needs.
+ * each kernel launched as the programmatic dependent of the one before it: a large projection
+ * (step 2, more than 8 GFLOP) is launched first and the top-k (step 1) runs beside it; a
+ * smaller projection is launched after the top-k and runs on the SMs the top-k's first
+ * finished CTAs leave. The edges (step 3) take the SMs the top-k leaves as it finishes,
+ * scoring each (r, p) tile as soon as the top-k has written the rows it needs and the
+ * projection is done. The results do not depend on the order.
  * The call returns once everything is enqueued; later work on `stream` sees all outputs. It is
  * safe to capture in a CUDA graph; make one call on the device before capturing. The
  * workspace holds the top-k's and the edge tiles' bookkeeping (its size query includes
