@@ -440,16 +440,26 @@ def test_selector_large_full(dev, name):
 
 
 def test_selector_trace(dev):
+    """Traced calls time each stage, and give the same bits as untraced ones: a traced call
+    runs the projection first and the kernels one after another, while an untraced call at
+    this size launches the projection after the top-k."""
     inp = host_inputs("small_ties")
     w = inp.workload
     d = P.to_device(inp, dev)
+    args = (d["logits"], d["hidden"], d["w_proj"], d["pred_cb"], d["succ_cb"], d["anchors"], w.K)
+    untraced = [x.clone() for x in ds.dflash_selector(*args)]
     ds.dflash_trace_begin(3)
+    outs = []
     for _ in range(4):   # the fourth call is beyond the trace capacity and not traced
-        ds.dflash_selector(d["logits"], d["hidden"], d["w_proj"], d["pred_cb"], d["succ_cb"],
-                           d["anchors"], w.K)
+        outs.append([x.clone() for x in ds.dflash_selector(*args)])
     stages = ds.dflash_trace_end(8)
     assert len(stages) == 3
     assert all(t >= 0 for row in stages for t in row) and all(row[1] > 0 for row in stages)
+    bits = {torch.bfloat16: torch.int16, torch.float32: torch.int32, torch.int32: torch.int32}
+    for o in outs:
+        for a, b in zip(o, untraced):
+            assert torch.equal(a.view(bits[a.dtype]), b.view(bits[b.dtype]))
+    _status_clean()
 
 
 def test_selector_cuda_graph_replay(dev):
