@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--requests R] [--e2e-steps E] [--graph]
                     [--no-cpu-baseline] [--no-per-workload]
-    python bench.py --forward | --lmhead [--sustained SECONDS] | --best-path  [--workload NAME]
+    python bench.py --forward | --lmhead [--sustained SECONDS | --lmhead-only] | --best-path
+                    [--workload NAME]
 
 One step is one dflash_selector call over one batch of the workload: vocabulary top-k,
 hidden projection and edge scores, with every input already in HBM. The default
@@ -735,6 +736,17 @@ def run_lmhead(args, w: wl.Workload) -> None:
     with ClockSampler(dev) as clocks:
         ms = timed(step, args.steps)
     status = ds.dflash_device_status(clear=True)
+    if args.lmhead_only:
+        # The LM-head top-k alone (hidden states and the LM head on the device, nothing else):
+        # the small footprint a profiler capture of this kernel wants.
+        print(json.dumps({
+            "metric": "candidate-head rows/s from the LM head (R*S)", "value": w.rows / (ms / 1e3),
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16 x bf16 -> f32",
+            "data": "synthetic (seeded)", "config": base_config(w, 1),
+            "gpu_launches": args.steps, "device_status": status, "clocks": clocks.summary(),
+        }), flush=True)
+        return
     h2 = hidden.reshape(w.rows, w.H)
     gemm_ms = timed(lambda: torch.matmul(h2, lm_head.t()), max(3, args.steps // 4))
     logits = torch.empty((w.R, w.S, w.V), dtype=torch.float32, device=dev).normal_()
@@ -890,6 +902,9 @@ def main(argv=None) -> None:
                     help="skip the forward pass and the other workloads after the headline")
     ap.add_argument("--lmhead", action="store_true",
                     help="time the candidate head straight from a synthetic LM head instead")
+    ap.add_argument("--lmhead-only", action="store_true",
+                    help="with --lmhead: the LM-head top-k alone, without the unfused route, "
+                         "the draft step or the end-to-end timing")
     ap.add_argument("--sustained", type=float, default=0.0,
                     help="with --lmhead: also run the fused kernel and the cuBLAS GEMM back to "
                          "back for this many seconds each, sampling clocks and power")
