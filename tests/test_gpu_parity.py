@@ -886,6 +886,35 @@ def test_selector_lmhead(dev, R, S, K, V, H, rank, cap, scale):
     _status_clean()
 
 
+@pytest.mark.parametrize("name", ["qwen_zipf", "gemma_softcap"])
+def test_selector_lmhead_full_size(dev, name):
+    """The draft step from the LM head at full size (on 152 SMs its LM-head top-k runs on CTA
+    pairs at both shapes), with the workload's hidden states, projection and codebooks and a
+    seeded synthetic LM head: its candidates are those of dflash_lmhead_topk bit for bit and
+    valid on every row against fp32 logits; h and every edge score match the oracle on those
+    candidates."""
+    inp = host_inputs(name)
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    lm = (torch.randn((w.V, w.H), generator=g, device=dev) / w.H ** 0.5).to(torch.bfloat16)
+    ids, un, h, e = ds.dflash_selector_lmhead(d["hidden"], lm, d["w_proj"], d["pred_cb"],
+                                              d["succ_cb"], d["anchors"], w.K, softcap=w.softcap)
+    ids2, un2 = ds.dflash_lmhead_topk(d["hidden"], lm, w.K, softcap=w.softcap)
+    torch.cuda.synchronize(dev)
+    assert torch.equal(ids, ids2)
+    assert torch.equal(un.view(torch.int32), un2.view(torch.int32))
+    P.assert_lmhead_valid_every_row(ids, un, d["hidden"], lm, w.K, f"{name} draft step",
+                                    softcap=w.softcap)
+    P.assert_projection(P.bits(h), P.bits(inp.hidden), P.bits(inp.w_proj), f"{name} h")
+    ref_e = oracle.edges(P.bits(inp.pred_cb), P.bits(inp.succ_cb), ids.cpu().numpy(),
+                         un.cpu().numpy(), P.bits(h), inp.anchors)
+    P.assert_close(e.cpu().numpy(), ref_e, f"{name} edges")
+    del d, lm
+    _status_clean()
+
+
 def test_wait_timeout_is_reported_and_the_context_survives(dev):
     """The failure path of the bounded waits, without a fault: a wait on an mbarrier that
     nothing arrives on, then an edge CTA's wait in the fused selector's ready queue for a tile
