@@ -573,6 +573,31 @@ def test_selector_forward(dev, name):
     _status_clean()
 
 
+@pytest.mark.parametrize("name", LARGE)
+def test_selector_forward_full_size(dev, name):
+    """The forward pass at full size in the launch configuration `bench.py --forward` times
+    (gemma_large: the projection on 30 CTA pairs split over K in two, the edges launched as its
+    programmatic dependent), on the workload's inputs and seeded candidates with a repeat in
+    every row: every entry of h and every edge score against the oracle."""
+    inp = host_inputs(name)
+    w = inp.workload
+    d = P.to_device(inp, dev)
+    rng = np.random.default_rng(23)
+    cand = rng.integers(0, w.V, size=(w.R, w.S, w.K)).astype(np.int32)
+    cand[:, :, -1] = cand[:, :, 0]
+    unary = rng.standard_normal((w.R, w.S, w.K)).astype(np.float32)
+    h, e = ds.dflash_selector_forward(torch.from_numpy(cand).to(dev),
+                                      torch.from_numpy(unary).to(dev), d["hidden"],
+                                      d["anchors"], d["w_proj"], d["pred_cb"], d["succ_cb"])
+    torch.cuda.synchronize(dev)
+    P.assert_projection(P.bits(h), P.bits(inp.hidden), P.bits(inp.w_proj), f"{name} forward h")
+    ref = oracle.edges(P.bits(inp.pred_cb), P.bits(inp.succ_cb), cand, unary, P.bits(h),
+                       inp.anchors)
+    P.assert_close(e.cpu().numpy(), ref, f"{name} forward edges")
+    del d
+    _status_clean()
+
+
 @pytest.mark.parametrize("R,S,K,V,H,rank", [(4, 15, 32, 50000, 5376, 256), (3, 7, 13, 40000, 520, 256)])
 def test_selector_forward_rank_256(dev, R, S, K, V, H, rank):
     """The forward pass at a rank of 256, where the projection runs on CTA pairs with a K
